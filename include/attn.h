@@ -1,0 +1,137 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) fused attention forward library
+ * (libattn_sm103.so).
+ *
+ * The operation (one call = one whole forward pass over every (b, h)):
+ *
+ *     S   = scale * Q K^T           (per head; K^T is the transpose of K)
+ *     S   = -inf where key j > query i           (only when causal != 0)
+ *     O   = softmax_rows(S) V
+ *     LSE = log(sum_j exp(S_ij))    (natural log, per query row)
+ *
+ * computed block by block with the online softmax (running row max and row
+ * sum, rescale of the partial output when the max grows, division by the
+ * sum at the end) under a producer/consumer warp-specialised schedule.
+ * Source: "Warp specialization" concept card (wikillm), sections
+ * "Implementation sketch" (the consumer loop and its return value: output /
+ * row_sum and row_max + log(row_sum)) and "Variants" (producer/consumer
+ * roles, pingpong of two consumers); "Inside FlashAttention-3 &
+ * Warp-Specialized CUDA Kernels" (tekromancy), sections 2 and 4 (TMA ring
+ * with mbarriers, tcgen05.mma into Tensor Memory).  The pages leave the
+ * scale, the mask convention and the layout open; this library takes:
+ *   - scale multiplies Q K^T before the mask, the max and the exponential,
+ *     so LSE is in units of the scaled scores;
+ *   - causal: key j is visible to query i iff j <= i (square, top-left);
+ *   - layout below.
+ *
+ * Layout.  Q, K, V and O are dense row-major [B, H, N, d] tensors (d
+ * fastest), all with the same N (self-attention shape).  LSE is a dense
+ * [B, H, N] fp32 tensor.  O has the input element type, except for e4m3
+ * inputs, whose O is bf16.
+ *
+ * Memory.  Every pointer is a DEVICE pointer on the current CUDA device,
+ * owned by the caller.  The library allocates and frees nothing and keeps
+ * no state between calls apart from one device-side watchdog word per
+ * device (see attn_fwd_status).  Inputs are only read; O and LSE are only
+ * written, every element once.
+ *
+ * Asynchrony.  Calls enqueue one kernel on `stream` (NULL = the legacy
+ * default stream) and return; results are valid once the stream has
+ * synchronised.  Calls on different streams may run concurrently.
+ *
+ * Errors.  Every argument check runs before anything is enqueued; a call
+ * that fails a check returns a nonzero attn_status_t and has no side
+ * effects.  A failed kernel launch returns ATTN_ERR_CUDA.
+ */
+#ifndef WS_ATTN_H_
+#define WS_ATTN_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream type (cudaStream_t is a pointer to this). */
+struct CUstream_st;
+
+typedef enum {
+    ATTN_FP32 = 0,      /* fp32 in, fp32 out; the matrix products run in tf32 */
+    ATTN_FP16 = 1,      /* fp16 in, fp16 out, fp32 accumulation */
+    ATTN_BF16 = 2,      /* bf16 in, bf16 out, fp32 accumulation */
+    ATTN_FP8_E4M3 = 3   /* e4m3 in (descales 1.0 through attn_fwd), bf16 out */
+} attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, bad scale/causal/dtype */
+    ATTN_ERR_UNSUPPORTED = 2,   /* head dim not built for this dtype, or kernel not runnable */
+    ATTN_ERR_MISALIGNED = 3,    /* q/k/v/o not 16-byte aligned, or lse not 4-byte aligned */
+    ATTN_ERR_DEVICE = 4,        /* no CUDA device, or the current device is not sm_103 */
+    ATTN_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+    ATTN_ERR_TIMEOUT = 6        /* a device-side wait exceeded its limit (see attn_fwd_status) */
+} attn_status_t;
+
+/*
+ * attn_fwd - one forward pass.
+ *   q, k, v : [B, H, N, d] device tensors of `dtype`, 16-byte aligned.
+ *   o       : [B, H, N, d] device output (dtype; bf16 for ATTN_FP8_E4M3),
+ *             16-byte aligned.
+ *   lse     : [B, H, N] fp32 device output, 4-byte aligned.
+ *   B, H    : >= 1, B*H <= 2^24.
+ *   N       : 1 <= N <= 2^24 and B*H*N <= 2^31 - 1; a final partial block
+ *             of 128 keys is masked.
+ *   d       : 64, 128 or 256 for fp16/bf16; 64 or 128 for fp32 and 128
+ *             for e4m3.
+ *   scale   : finite and > 0 (usually 1/sqrt(d)).
+ *   causal  : 0 or 1.
+ *   dtype   : an attn_dtype_t.
+ * Returns ATTN_OK or an attn_status_t error code.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int N, int d, float scale, int causal, int dtype,
+             struct CUstream_st* stream);
+
+/*
+ * attn_fwd_fp8 - forward pass on e4m3 inputs quantised with per-tensor
+ * scales: the real values are code * descale.  q_descale * k_descale is
+ * folded into the softmax scale and v_descale is applied to O before the
+ * bf16 rounding.  The probabilities are re-quantised to e4m3 (scale 1)
+ * for the P.V product; the row sum uses them before that rounding.
+ * Source: tekromancy page, section 5 (FP8 E4M3 forward; per-tensor
+ * scaling).  Arguments as attn_fwd with dtype ATTN_FP8_E4M3 (d = 128); the
+ * descales must be finite and > 0.
+ */
+int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int causal,
+                 float q_descale, float k_descale, float v_descale,
+                 struct CUstream_st* stream);
+
+/*
+ * attn_fwd_status - synchronises `stream`, then reports and clears the
+ * device watchdog word of the current device.  Every wait inside the
+ * kernels is bounded (about two seconds); a wait that runs out records
+ * ATTN_ERR_TIMEOUT there and the kernel ends without writing the rest of
+ * its outputs.  Returns ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA if
+ * the synchronisation itself reports an error.
+ */
+int attn_fwd_status(struct CUstream_st* stream);
+
+/* attn_status_string - a static, human-readable name for a status code. */
+const char* attn_status_string(int status);
+
+/*
+ * attn_watchdog_selftest - checks the watchdog path itself on the device:
+ * launches one CTA that waits on an mbarrier nobody arrives on, with a
+ * limit of `timeout_us` microseconds (1 .. 10^7).  The wait runs out, the
+ * kernel records ATTN_ERR_TIMEOUT in the watchdog word and returns.  This
+ * call then synchronises `stream` and returns what attn_fwd_status would
+ * (ATTN_ERR_TIMEOUT when the watchdog works), clearing the word.  Not part
+ * of the attention computation; it exists so the bounded-wait mechanism
+ * can be tested without a real fault.
+ */
+int attn_watchdog_selftest(unsigned int timeout_us, struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WS_ATTN_H_ */

@@ -1,0 +1,171 @@
+"""Python binding of libattn_sm103.so, the GB300 (sm_103a) fused attention
+forward library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  The functions take torch CUDA tensors for convenience (torch is
+used for device memory and streams) and pass raw device pointers through the
+C ABI of include/attn.h.  There is no fallback: if the library is missing or
+the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "ATTN_FP32", "ATTN_FP16", "ATTN_BF16", "ATTN_FP8_E4M3", "AttnError", "lib_path",
+    "load_library", "attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
+    "attn_watchdog_selftest", "attn_fwd_raw", "EXPORTED_SYMBOLS",
+]
+
+ATTN_FP32, ATTN_FP16, ATTN_BF16, ATTN_FP8_E4M3 = 0, 1, 2, 3
+
+STATUS_NAMES = {
+    0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+    3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_DEVICE", 5: "ATTN_ERR_CUDA", 6: "ATTN_ERR_TIMEOUT",
+}
+
+EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
+                    "attn_watchdog_selftest")
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = "attn_fwd"):
+        self.status = int(status)
+        super().__init__(f"{what} failed: {STATUS_NAMES.get(self.status, self.status)}")
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "_build", "libattn_sm103.so")
+
+
+def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load the shared library (optionally building it first)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = lib_path()
+        if build_if_missing:
+            from . import build as _build
+            path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m warp_specialized_gb300.build` "
+                "(there is no fallback implementation)")
+        lib = ctypes.CDLL(path)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.attn_fwd.restype = i
+        lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, f, f, f, vp]
+        lib.attn_fwd_fp8.restype = i
+        lib.attn_fwd_status.argtypes = [vp]
+        lib.attn_fwd_status.restype = i
+        lib.attn_status_string.argtypes = [i]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_watchdog_selftest.argtypes = [ctypes.c_uint, vp]
+        lib.attn_watchdog_selftest.restype = i
+        _lib = lib
+        return lib
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _dtype_code(t):
+    import torch
+    codes = {torch.float32: ATTN_FP32, torch.float16: ATTN_FP16, torch.bfloat16: ATTN_BF16,
+             torch.float8_e4m3fn: ATTN_FP8_E4M3}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int,
+                 N: int, d: int, scale: float, causal: bool, dtype: int, stream: int = 0) -> int:
+    """The C call with raw device pointers; returns the status code."""
+    return load_library().attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d,
+                                   float(scale), int(bool(causal)), int(dtype), stream)
+
+
+def _check_qkv(q, k, v):
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share one dtype")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+
+
+def attn_fwd(q, k, v, scale=None, causal: bool = False, out=None, lse=None, stream=None):
+    """O, LSE = attention forward of [B, H, N, d] CUDA tensors.
+
+    scale defaults to 1/sqrt(d).  out / lse may be given preallocated
+    ([B, H, N, d] of q's dtype, [B, H, N] fp32).  Asynchronous on `stream`
+    (default: torch's current stream).  Returns (out, lse)."""
+    import torch
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    code = _dtype_code(q)
+    out_dtype = torch.bfloat16 if code == ATTN_FP8_E4M3 else q.dtype
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      B, H, N, d, scale, causal, code, _stream_handle(stream))
+    if st != 0:
+        raise AttnError(st)
+    return out, lse
+
+
+def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, scale=None,
+                 causal: bool = False, out=None, lse=None, stream=None):
+    """Forward pass on e4m3 tensors with per-tensor descales; O is bf16."""
+    import torch
+    _check_qkv(q, k, v)
+    if q.dtype != torch.float8_e4m3fn:
+        raise TypeError("attn_fwd_fp8 takes float8_e4m3fn tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st = load_library().attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
+                                     float(q_descale), float(k_descale), float(v_descale),
+                                     _stream_handle(stream))
+    if st != 0:
+        raise AttnError(st, "attn_fwd_fp8")
+    return out, lse
+
+
+def attn_fwd_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device watchdog status."""
+    return int(load_library().attn_fwd_status(_stream_handle(stream)))
+
+
+def attn_watchdog_selftest(timeout_us: int = 2000, stream=None) -> int:
+    """Run the watchdog self-test kernel; returns ATTN_ERR_TIMEOUT (6) when the
+    bounded wait works."""
+    return int(load_library().attn_watchdog_selftest(int(timeout_us), _stream_handle(stream)))

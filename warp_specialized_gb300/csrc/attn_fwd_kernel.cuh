@@ -1,0 +1,765 @@
+// attn_fwd_kernel.cuh - the warp-specialised fused attention forward kernel
+// for sm_103a (GB300).
+//
+// What it computes, per (b, h) and query row i (natural-log LSE):
+//   S = scale * Q K^T, masked (-inf) where key > query when causal and
+//   where key >= N; O = softmax(S) V; LSE = log sum exp S.
+// It walks the key/value blocks j with the online softmax of the
+// "Warp specialization" concept card (wikillm), section "Implementation
+// sketch": running row max m and row sum l, the old sum and output rescaled
+// by exp(m_old - m_new) (the card's form, not the inverse factor it
+// rejects), O / l and m + log l at the end.
+//
+// Schedule (GB300 form of the producer/consumer split of the card's
+// "Variants" section and of the tekromancy page, sections 1-4):
+//   warp 0        producer: one thread streams Q tiles and the K_j / V_j
+//                 tiles into a shared-memory ring with TMA; every ring slot
+//                 has a "full" mbarrier (TMA transaction bytes) and an
+//                 "empty" mbarrier (released by the MMA commit).
+//   warp 1        MMA issuer: one thread issues tcgen05.mma; S = Q K_j^T
+//                 lands in Tensor Memory, O += P V_j accumulates there with
+//                 P read from Tensor Memory.
+//   warps 4-7     softmax of query tile A, one thread per row (lane) of the
+//                 128-row tile: row max, exp2, row sum, P written back over
+//                 S in Tensor Memory (no shuffles: a row lives in one
+//                 thread, spheron page, section on Blackwell).
+//   warps 8-11    softmax of query tile B.  The MMA thread alternates
+//                 between the two tiles (S_A, S_B, PV_A, S_A', PV_B, S_B',
+//                 ...), so the exponentials of one tile overlap the matrix
+//                 products of the other: the two-consumer pingpong of the
+//                 card's "Pingpong scheduling" variant, with the turn-taking
+//                 done by the MMA issue order instead of named barriers.
+//   warps 12-15   correction and epilogue: rescales O in Tensor Memory by
+//                 exp2(m_old - m_new) when a row max grew, and at the end
+//                 writes O / l and lets the softmax warps write LSE.
+// The grid is persistent (one CTA per SM); CTAs walk a static list of
+// (head, pair of query tiles) work items.  With the causal mask blocks
+// above the diagonal are never loaded or multiplied, and the list starts
+// with the items that have the most blocks.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx_sm103.cuh"
+
+namespace wsattn {
+
+// status codes mirrored from attn.h (kept numerically identical)
+constexpr unsigned kStatusTimeout = 6u;
+
+// element types: 0 fp32 (tf32 products), 1 fp16, 2 bf16, 3 e4m3
+template <int DT>
+struct DTypeTraits;
+template <>
+struct DTypeTraits<0> {
+  static constexpr int kEsize = 4;
+  static constexpr uint32_t kFmt = 2;  // tf32
+  static constexpr MmaKind kKind = MmaKind::kTF32;
+  static constexpr int kOutEsize = 4;
+};
+template <>
+struct DTypeTraits<1> {
+  static constexpr int kEsize = 2;
+  static constexpr uint32_t kFmt = 0;  // f16
+  static constexpr MmaKind kKind = MmaKind::kF16;
+  static constexpr int kOutEsize = 2;
+};
+template <>
+struct DTypeTraits<2> {
+  static constexpr int kEsize = 2;
+  static constexpr uint32_t kFmt = 1;  // bf16
+  static constexpr MmaKind kKind = MmaKind::kF16;
+  static constexpr int kOutEsize = 2;
+};
+template <>
+struct DTypeTraits<3> {
+  static constexpr int kEsize = 1;
+  static constexpr uint32_t kFmt = 0;  // e4m3
+  static constexpr MmaKind kKind = MmaKind::kF8F6F4;
+  static constexpr int kOutEsize = 2;  // bf16 output
+};
+
+constexpr int kThreads = 512;
+constexpr int kBlock = 128;            // query rows per tile = keys per block
+constexpr int kSmemLimit = 232448;     // opt-in shared memory per block on sm_100/sm_103
+constexpr int kMaxSlots = 8;
+
+template <int DT, int D>
+struct Cfg {
+  using T = DTypeTraits<DT>;
+  static constexpr int kEsize = T::kEsize;
+  static constexpr int kRowBytes = D * kEsize;
+  static constexpr int kBoxInner = 128 / kEsize;     // elements per 128-byte swizzled row
+  static constexpr int kNumBox = kRowBytes / 128;    // TMA boxes per tile
+  static constexpr int kBoxBytes = kBlock * 128;     // 16 KiB
+  static constexpr int kTileBytes = kNumBox * kBoxBytes;
+  // two query tiles per CTA when both S and O of both fit in Tensor Memory
+  // (2 * (128 + D) <= 512 columns) and in shared memory
+  static constexpr int kNQT = (D <= 128 && kTileBytes <= 32768) ? 2 : 1;
+  static constexpr int kMiscBytes = 1024 /*alignment*/ + 512 /*barriers*/ +
+                                    2 * kBlock * 4 /*alpha*/ + 2 * 2 * kBlock * 4 /*1/l*/;
+  static constexpr int kSlotsFit = (kSmemLimit - kMiscBytes - kNQT * kTileBytes) / kTileBytes;
+  static constexpr int kSlots = kSlotsFit > kMaxSlots ? kMaxSlots : kSlotsFit;
+  static_assert(kSlots >= 2, "the K/V ring needs at least two slots");
+  static constexpr int kSmemBytes = kMiscBytes + (kNQT + kSlots) * kTileBytes;
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
+  static_assert(kNQT * kTileBytes % 1024 == 0 && kTileBytes % 1024 == 0, "tile alignment");
+  static_assert(kRowBytes % 128 == 0, "head dim must fill whole 128-byte swizzle rows");
+
+  // tensor-core shapes: M = 128 rows, K per instruction = 32 bytes
+  static constexpr int kKPerMma = 32 / kEsize;
+  static constexpr int kNumQKMma = kRowBytes / 32;
+  static constexpr int kNumPVMma = kBlock / kKPerMma;
+  static constexpr int kPCols = kBlock * kEsize / 4;  // TMEM columns holding P
+  static constexpr uint32_t kIdescQK = make_idesc(T::kFmt, T::kFmt, false, kBlock, kBlock);
+  static constexpr uint32_t kIdescPV = make_idesc(T::kFmt, T::kFmt, true, D, kBlock);
+
+  // Tensor Memory columns
+  static constexpr uint32_t kTmemCols = 512;
+  static __host__ __device__ constexpr uint32_t s_col(int t) { return t * kBlock; }
+  static __host__ __device__ constexpr uint32_t o_col(int t) { return kNQT * kBlock + t * D; }
+  static_assert(kNQT * (kBlock + D) <= 512, "Tensor Memory budget");
+};
+
+struct AttnParams {
+  void* o;
+  float* lse;
+  int N;
+  int BH;
+  int n_qt;       // query tiles per head
+  int n_pairs;    // work items per head (groups of kNQT query tiles)
+  int n_items;    // BH * n_pairs
+  int nkv;        // key blocks per head
+  float scale_log2;   // scale * (q, k descales) * log2(e)
+  float out_scale;    // v descale (1 for non-fp8)
+  unsigned long long timeout_ns;
+  // library-owned device words: the first error seen by any kernel, and a
+  // code saying which wait ran out (role * 16 + barrier kind)
+  unsigned int* status;
+  unsigned int* where;
+};
+
+struct Item {
+  int bh;
+  int qt0;
+  int n[2];
+  int nmax;
+};
+
+template <int NQT, bool CAUSAL>
+__device__ __forceinline__ Item decode_item(int it, const AttnParams& p) {
+  Item r;
+  int pair;
+  if (CAUSAL) {  // most blocks first
+    pair = p.n_pairs - 1 - it / p.BH;
+    r.bh = it % p.BH;
+  } else {
+    r.bh = it / p.n_pairs;
+    pair = it % p.n_pairs;
+  }
+  r.qt0 = pair * NQT;
+  r.nmax = 0;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    int qt = r.qt0 + t;
+    int n = CAUSAL ? min(qt + 1, p.nkv) : p.nkv;
+    r.n[t] = (t < NQT) ? n : 0;
+    r.nmax = max(r.nmax, r.n[t]);
+  }
+  return r;
+}
+
+// Shared-memory control block (after the tiles).
+template <int NSLOT>
+struct Ctrl {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[NSLOT], kv_empty[NSLOT];
+  uint64_t s_full[2];    // S_t(j) in TMEM            (MMA commit)
+  uint64_t p_full[2];    // P_t(j) in TMEM            (4 softmax warps)
+  uint64_t sc_full[2];   // alpha_t(j) in smem        (4 softmax warps)
+  uint64_t o_full[2];    // PV_t(j) done              (MMA commit)
+  uint64_t o_ready[2];   // O_t rescaled for block j  (4 correction warps)
+  uint64_t drain;        // all MMAs done             (MMA commit)
+  uint32_t tmem_base;
+  uint32_t abort;        // set when a wait in this CTA ran out
+  float alpha[2][kBlock];
+  float inv_l[2][2][kBlock];  // [item parity][tile][row]
+};
+
+// Bounded wait: true when the phase with `parity` has completed; false when
+// another thread of this CTA gave up or the limit ran out (then the status
+// word records a timeout and `where`).
+struct WaitCtx {
+  volatile uint32_t* abort;
+  unsigned long long limit_ns;
+  unsigned int* status;
+  unsigned int* where;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx& wc,
+                                        unsigned where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*wc.abort) return false;
+    if (global_timer_ns() - t0 > wc.limit_ns) {
+      *wc.abort = 1u;
+      atomicCAS(wc.status, 0u, kStatusTimeout);
+      atomicExch(wc.where, where);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// producer: Q tiles, then K_j and V_j through the ring
+
+template <int DT, int D, bool CAUSAL>
+__device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                              const CUtensorMap* tmV, uint8_t* sbase,
+                              Ctrl<Cfg<DT, D>::kSlots>* c, const AttnParams& p) {
+  using C = Cfg<DT, D>;
+  const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
+  const uint8_t* sq = sbase;
+  const uint8_t* skv = sbase + C::kNQT * C::kTileBytes;
+  uint32_t q_uses[2] = {0, 0};
+  int slot = 0;
+  uint32_t round = 0;
+  uint32_t loads = 0;  // total ring loads issued
+  bool ok = true;
+
+  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+    const Item w = decode_item<C::kNQT, CAUSAL>(it, p);
+#pragma unroll
+    for (int t = 0; t < C::kNQT; ++t) {
+      const uint32_t full = smem_u32(&c->q_full[t]);
+      if (!wait_bar(smem_u32(&c->q_empty[t]), (q_uses[t] & 1u) ^ 1u, wc, 0x01)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(full, C::kTileBytes);
+      const uint32_t dst = smem_u32(sq + t * C::kTileBytes);
+#pragma unroll
+      for (int b = 0; b < C::kNumBox; ++b)
+        tma_load_3d(dst + b * C::kBoxBytes, tmQ, b * C::kBoxInner, (w.qt0 + t) * kBlock, w.bh, full);
+      ++q_uses[t];
+    }
+    for (int j = 0; j < w.nmax && ok; ++j) {
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        if (!wait_bar(smem_u32(&c->kv_empty[slot]), (round & 1u) ^ 1u, wc, 0x02)) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = smem_u32(&c->kv_full[slot]);
+        mbar_arrive_expect_tx(full, C::kTileBytes);
+        const uint32_t dst = smem_u32(skv + slot * C::kTileBytes);
+        const CUtensorMap* map = kv == 0 ? tmK : tmV;
+#pragma unroll
+        for (int b = 0; b < C::kNumBox; ++b)
+          tma_load_3d(dst + b * C::kBoxBytes, map, b * C::kBoxInner, j * kBlock, w.bh, full);
+        ++loads;
+        if (++slot == C::kSlots) {
+          slot = 0;
+          ++round;
+        }
+      }
+    }
+  }
+  // Never leave a copy in flight: wait until the last load of every slot
+  // and of every Q tile has landed (immediate on the normal path).
+  for (int s = 0; s < C::kSlots; ++s) {
+    const uint32_t uses = loads / C::kSlots + (static_cast<uint32_t>(s) < loads % C::kSlots ? 1u : 0u);
+    if (uses) {
+      volatile uint32_t never = 0;
+      const WaitCtx wc_never{&never, p.timeout_ns, p.status, p.where};
+      wait_bar(smem_u32(&c->kv_full[s]), (uses - 1u) & 1u, wc_never, 0x03);
+    }
+  }
+  for (int t = 0; t < C::kNQT; ++t) {
+    if (q_uses[t]) {
+      volatile uint32_t never = 0;
+      const WaitCtx wc_never{&never, p.timeout_ns, p.status, p.where};
+      wait_bar(smem_u32(&c->q_full[t]), (q_uses[t] - 1u) & 1u, wc_never, 0x04);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread)
+
+template <int DT, int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk) {
+  using C = Cfg<DT, D>;
+#pragma unroll
+  for (int k = 0; k < C::kNumQKMma; ++k) {
+    const uint32_t off = (k >> 2) * C::kBoxBytes + (k & 3) * 32;
+    const uint64_t a = make_sdesc_sw128(sq + off, 16, 1024);
+    const uint64_t b = make_sdesc_sw128(sk + off, 16, 1024);
+    mma_ss<C::T::kKind>(d_tmem, a, b, C::kIdescQK, k > 0 ? 1u : 0u);
+  }
+}
+
+template <int DT, int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t sv,
+                                         bool accumulate) {
+  using C = Cfg<DT, D>;
+#pragma unroll
+  for (int k = 0; k < C::kNumPVMma; ++k) {
+    // V is [keys, d] with d contiguous: an MN-major B operand.  Each 8-key
+    // group is one 1024-byte swizzle atom (SBO); 128-byte column blocks of d
+    // are one TMA box apart (LBO).
+    const uint64_t b = make_sdesc_sw128(sv + k * C::kKPerMma * 128, C::kBoxBytes, 1024);
+    mma_ts<C::T::kKind>(d_tmem, p_tmem + k * 8, b, C::kIdescPV, (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
+template <int DT, int D, bool CAUSAL>
+__device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
+                         const AttnParams& p) {
+  using C = Cfg<DT, D>;
+  constexpr int NQT = C::kNQT;
+  const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
+  const uint32_t sq = smem_u32(sbase);
+  const uint32_t skv = sq + NQT * C::kTileBytes;
+  uint32_t q_waits[2] = {0, 0}, p_waits[2] = {0, 0}, r_waits[2] = {0, 0};
+  int slot = 0;
+  uint32_t round = 0;
+  bool ok = true;
+
+  auto next_slot = [&](int& s, uint32_t& par) {
+    s = slot;
+    par = round & 1u;
+    if (++slot == C::kSlots) {
+      slot = 0;
+      ++round;
+    }
+  };
+
+  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+    const Item w = decode_item<NQT, CAUSAL>(it, p);
+    // S_t(0) for every tile
+    int ks;
+    uint32_t kpar;
+    next_slot(ks, kpar);
+    if (!wait_bar(smem_u32(&c->kv_full[ks]), kpar, wc, 0x11)) break;
+    for (int t = 0; t < NQT && ok; ++t) {
+      if (!wait_bar(smem_u32(&c->q_full[t]), q_waits[t] & 1u, wc, 0x12)) {
+        ok = false;
+        break;
+      }
+      ++q_waits[t];
+      tc_fence_after_sync();
+      issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes, skv + ks * C::kTileBytes);
+      mma_commit(smem_u32(&c->s_full[t]));
+      if (w.n[t] == 1) mma_commit(smem_u32(&c->q_empty[t]));
+    }
+    if (!ok) break;
+    mma_commit(smem_u32(&c->kv_empty[ks]));
+
+    for (int j = 0; j < w.nmax && ok; ++j) {
+      int vs;
+      uint32_t vpar;
+      next_slot(vs, vpar);
+      if (!wait_bar(smem_u32(&c->kv_full[vs]), vpar, wc, 0x13)) break;
+      const bool have_next = j + 1 < w.nmax;
+      int ns = 0;
+      uint32_t npar = 0;
+      bool k_ready = false;
+      if (have_next) next_slot(ns, npar);
+      for (int t = 0; t < NQT && ok; ++t) {
+        if (j < w.n[t]) {
+          if (!wait_bar(smem_u32(&c->p_full[t]), p_waits[t] & 1u, wc, 0x14) ||
+              !wait_bar(smem_u32(&c->o_ready[t]), r_waits[t] & 1u, wc, 0x15)) {
+            ok = false;
+            break;
+          }
+          ++p_waits[t];
+          ++r_waits[t];
+          tc_fence_after_sync();
+          issue_pv<DT, D>(tbase + C::o_col(t), tbase + C::s_col(t), skv + vs * C::kTileBytes,
+                          j > 0);
+          mma_commit(smem_u32(&c->o_full[t]));
+        }
+        if (j + 1 < w.n[t]) {
+          if (!k_ready) {
+            if (!wait_bar(smem_u32(&c->kv_full[ns]), npar, wc, 0x16)) {
+              ok = false;
+              break;
+            }
+            k_ready = true;
+          }
+          issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes, skv + ns * C::kTileBytes);
+          mma_commit(smem_u32(&c->s_full[t]));
+          if (j + 2 == w.n[t]) mma_commit(smem_u32(&c->q_empty[t]));
+        }
+      }
+      if (!ok) break;
+      mma_commit(smem_u32(&c->kv_empty[vs]));
+      if (have_next) mma_commit(smem_u32(&c->kv_empty[ns]));
+    }
+  }
+  // Wait until every MMA issued above has completed before the CTA frees
+  // Tensor Memory.
+  mma_commit(smem_u32(&c->drain));
+  volatile uint32_t never = 0;
+  const WaitCtx wc_never{&never, p.timeout_ns, p.status, p.where};
+  wait_bar(smem_u32(&c->drain), 0u, wc_never, 0x17);
+}
+
+// ---------------------------------------------------------------------------
+// softmax warpgroup of tile t: one thread = one row = one TMEM lane
+
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<1>(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<2>(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// two e4m3 codes in the low 16 bits: a in the low byte
+__device__ __forceinline__ uint32_t pack2_e4m3(float a, float b) {
+  __nv_fp8x2_e4m3 v(make_float2(a, b));
+  return static_cast<uint32_t>(*reinterpret_cast<uint16_t*>(&v));
+}
+
+// Exponentials of 64 scores of one row, written as P into Tensor Memory
+// (the P columns of this half: 16-bit types pack two per column, e4m3 four,
+// tf32 one).  Returns the sum of the fp32 exponentials (before rounding).
+template <int DT>
+__device__ __forceinline__ float exp_store_half(const float (&s)[64], float sl2, float neg_m,
+                                                uint32_t taddr_p) {
+  float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+  if constexpr (DT == 0) {
+    uint32_t pk[64];
+#pragma unroll
+    for (int i = 0; i < 64; i += 4) {
+      const float e0 = ex2_approx(fmaf(s[i + 0], sl2, neg_m));
+      const float e1 = ex2_approx(fmaf(s[i + 1], sl2, neg_m));
+      const float e2 = ex2_approx(fmaf(s[i + 2], sl2, neg_m));
+      const float e3 = ex2_approx(fmaf(s[i + 3], sl2, neg_m));
+      sum0 += e0;
+      sum1 += e1;
+      sum2 += e2;
+      sum3 += e3;
+      pk[i + 0] = __float_as_uint(e0);
+      pk[i + 1] = __float_as_uint(e1);
+      pk[i + 2] = __float_as_uint(e2);
+      pk[i + 3] = __float_as_uint(e3);
+    }
+    tmem_st_x64(taddr_p, pk);
+  } else if constexpr (DT == 3) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 64; i += 4) {
+      const float e0 = ex2_approx(fmaf(s[i + 0], sl2, neg_m));
+      const float e1 = ex2_approx(fmaf(s[i + 1], sl2, neg_m));
+      const float e2 = ex2_approx(fmaf(s[i + 2], sl2, neg_m));
+      const float e3 = ex2_approx(fmaf(s[i + 3], sl2, neg_m));
+      sum0 += e0;
+      sum1 += e1;
+      sum2 += e2;
+      sum3 += e3;
+      pk[i / 4] = pack2_e4m3(e0, e1) | (pack2_e4m3(e2, e3) << 16);
+    }
+    tmem_st_x16(taddr_p, pk);
+  } else {
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < 64; i += 4) {
+      const float e0 = ex2_approx(fmaf(s[i + 0], sl2, neg_m));
+      const float e1 = ex2_approx(fmaf(s[i + 1], sl2, neg_m));
+      const float e2 = ex2_approx(fmaf(s[i + 2], sl2, neg_m));
+      const float e3 = ex2_approx(fmaf(s[i + 3], sl2, neg_m));
+      sum0 += e0;
+      sum1 += e1;
+      sum2 += e2;
+      sum3 += e3;
+      pk[i / 2] = pack2<DT>(e0, e1);
+      pk[i / 2 + 1] = pack2<DT>(e2, e3);
+    }
+    tmem_st_x32(taddr_p, pk);
+  }
+  return (sum0 + sum1) + (sum2 + sum3);
+}
+
+// Loads 64 scores (columns col0 .. col0+63 of the row) and applies the mask:
+// key columns at or past `lim` become -inf.
+__device__ __forceinline__ void load_scores_half(uint32_t taddr, int col0, int lim,
+                                                 float (&s)[64]) {
+  uint32_t raw[64];
+  tmem_ld_x64(taddr + col0, raw);
+#pragma unroll
+  for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(raw[i]);
+  if (lim < col0 + 64) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) s[i] = (col0 + i < lim) ? s[i] : -INFINITY;
+  }
+}
+
+template <int DT, int D, bool CAUSAL>
+__device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
+                             const AttnParams& p) {
+  using C = Cfg<DT, D>;
+  const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
+  const uint32_t lane = lane_id();
+  const uint32_t wq = (threadIdx.x >> 5) & 3u;  // warp quarter = TMEM lane group
+  const int r = static_cast<int>(wq * 32u + lane);
+  const uint32_t taddr = tbase + ((wq * 32u) << 16) + C::s_col(t);
+  const float sl2 = p.scale_log2;
+  uint32_t s_waits = 0;
+  uint32_t iter = 0;
+
+  for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++iter) {
+    const Item w = decode_item<C::kNQT, CAUSAL>(it, p);
+    const int qt = w.qt0 + t;
+    const int n = w.n[t];
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    for (int j = 0; j < n; ++j) {
+      if (!wait_bar(smem_u32(&c->s_full[t]), s_waits & 1u, wc, 0x21)) return;
+      ++s_waits;
+      tc_fence_after_sync();
+      // mask: keys >= N in the last block; keys after the query on the
+      // causal diagonal block
+      int lim = p.N - j * kBlock;
+      if (CAUSAL && j == qt) lim = min(lim, r + 1);
+
+      // Row max over the 128 scores, reading the upper half first so that
+      // the lower half is the one left in registers (a row of 128 fp32
+      // scores does not fit the 128-register budget of a 512-thread block
+      // together with its probabilities).
+      float s[64];
+      load_scores_half(taddr, 64, lim, s);
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, s[i]);
+      load_scores_half(taddr, 0, lim, s);
+#pragma unroll
+      for (int i = 0; i < 64; ++i) mx = fmaxf(mx, s[i]);
+
+      const float m_new = fmaxf(m_run, mx * sl2);
+      // subtraction reference: 0 while every key so far is masked
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      // rescale factor; exactly 1 when the max did not move, 0 on the
+      // first block (m_run = -inf)
+      const float alpha = m_run == m_use ? 1.0f : ex2_approx(m_run - m_use);
+      c->alpha[t][r] = alpha;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c->sc_full[t]));
+
+      // P over the first kPCols columns of S: the lower half's P lands on
+      // columns already read into registers, the upper half is re-read
+      // before its P overwrites anything it still needs.
+      const float neg_m = -m_use;
+      float sum = exp_store_half<DT>(s, sl2, neg_m, taddr);
+      load_scores_half(taddr, 64, lim, s);
+      sum += exp_store_half<DT>(s, sl2, neg_m, taddr + C::kPCols / 2);
+      l_run = alpha * l_run + sum;
+      m_run = m_new;
+      tmem_st_wait();
+      if (j == n - 1) {
+        // hand 1/l to the epilogue; write LSE (natural log) for real rows
+        c->inv_l[iter & 1u][t][r] = 1.0f / l_run;
+        const int row = qt * kBlock + r;
+        if (row < p.N)
+          p.lse[static_cast<size_t>(w.bh) * p.N + row] =
+              (m_use + log2f(l_run)) * 0.6931471805599453f;
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t]));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// correction / epilogue warpgroup
+
+template <int DT>
+__device__ __forceinline__ void store_out_chunk(void* dst, const float* v);  // 32 values
+
+template <>
+__device__ __forceinline__ void store_out_chunk<0>(void* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    d[i] = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                      __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+}
+template <>
+__device__ __forceinline__ void store_out_chunk<1>(void* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack2<1>(v[8 * i], v[8 * i + 1]), pack2<1>(v[8 * i + 2], v[8 * i + 3]),
+                      pack2<1>(v[8 * i + 4], v[8 * i + 5]), pack2<1>(v[8 * i + 6], v[8 * i + 7]));
+}
+template <>
+__device__ __forceinline__ void store_out_chunk<2>(void* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack2<2>(v[8 * i], v[8 * i + 1]), pack2<2>(v[8 * i + 2], v[8 * i + 3]),
+                      pack2<2>(v[8 * i + 4], v[8 * i + 5]), pack2<2>(v[8 * i + 6], v[8 * i + 7]));
+}
+template <>
+__device__ __forceinline__ void store_out_chunk<3>(void* dst, const float* v) {
+  store_out_chunk<2>(dst, v);
+}
+
+template <int DT, int D, bool CAUSAL>
+__device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, const AttnParams& p) {
+  using C = Cfg<DT, D>;
+  constexpr int NQT = C::kNQT;
+  const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
+  const uint32_t lane = lane_id();
+  const uint32_t wq = (threadIdx.x >> 5) & 3u;
+  const int r = static_cast<int>(wq * 32u + lane);
+  const uint32_t lane_off = (wq * 32u) << 16;
+  uint32_t sc_waits[2] = {0, 0}, o_waits[2] = {0, 0};
+  uint32_t iter = 0;
+
+  for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++iter) {
+    const Item w = decode_item<NQT, CAUSAL>(it, p);
+    for (int j = 0; j < w.nmax; ++j) {
+      for (int t = 0; t < NQT; ++t) {
+        if (j >= w.n[t]) continue;
+        if (!wait_bar(smem_u32(&c->sc_full[t]), sc_waits[t] & 1u, wc, 0x31))
+          return;
+        ++sc_waits[t];
+        const float alpha = c->alpha[t][r];
+        if (j > 0) {
+          if (!wait_bar(smem_u32(&c->o_full[t]), o_waits[t] & 1u, wc, 0x32))
+            return;
+          ++o_waits[t];
+          tc_fence_after_sync();
+          // exact skip: a warp whose 32 rows all kept their max has alpha == 1
+          if (!__all_sync(0xffffffffu, alpha == 1.0f)) {
+            const uint32_t ta = tbase + lane_off + C::o_col(t);
+#pragma unroll 1
+            for (int cc = 0; cc < D; cc += 32) {
+              uint32_t v[32];
+              tmem_ld_x32(ta + cc, v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              tmem_st_x32(ta + cc, v);
+            }
+            tmem_st_wait();
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&c->o_ready[t]));
+      }
+    }
+    // epilogue: O / l (times the v descale) -> output dtype, row by row
+    for (int t = 0; t < NQT; ++t) {
+      if (!wait_bar(smem_u32(&c->o_full[t]), o_waits[t] & 1u, wc, 0x33)) return;
+      ++o_waits[t];
+      tc_fence_after_sync();
+      const float f = c->inv_l[iter & 1u][t][r] * p.out_scale;
+      const int row = (w.qt0 + t) * kBlock + r;
+      const uint32_t ta = tbase + lane_off + C::o_col(t);
+      uint8_t* orow = static_cast<uint8_t*>(p.o) +
+                      (static_cast<size_t>(w.bh) * p.N + row) * D * C::T::kOutEsize;
+#pragma unroll 1
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t v[32];
+        tmem_ld_x32(ta + cc, v);
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]) * f;
+        if (row < p.N) store_out_chunk<DT>(orow + cc * C::T::kOutEsize, x);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+
+template <int DT, int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using C = Cfg<DT, D>;
+  using CtrlT = Ctrl<C::kSlots>;
+  static_assert(sizeof(CtrlT) + 1024 <= C::kMiscBytes, "control block budget");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // tiles need 1024-byte alignment (128-byte swizzle atoms)
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* sbase = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  CtrlT* c = reinterpret_cast<CtrlT*>(sbase + (C::kNQT + C::kSlots) * C::kTileBytes);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&c->q_full[t]), 1);
+      mbar_init(smem_u32(&c->q_empty[t]), 1);
+      mbar_init(smem_u32(&c->s_full[t]), 1);
+      mbar_init(smem_u32(&c->p_full[t]), 4);
+      mbar_init(smem_u32(&c->sc_full[t]), 4);
+      mbar_init(smem_u32(&c->o_full[t]), 1);
+      mbar_init(smem_u32(&c->o_ready[t]), 4);
+    }
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(smem_u32(&c->kv_full[s]), 1);
+      mbar_init(smem_u32(&c->kv_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&c->drain), 1);
+    c->abort = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&c->tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = c->tmem_base;
+
+  // Role dispatch by warpgroup.  Every thread keeps the launch's 128
+  // registers: ptxas allocates the whole kernel within the launch bound,
+  // so a setmaxnreg split would not give the softmax more to work with.
+  const uint32_t wg = warp >> 2;
+  if (wg == 0) {
+    if (warp == 0 && lane == 0)
+      role_producer<DT, D, CAUSAL>(&tmQ, &tmK, &tmV, sbase, c, p);
+    else if (warp == 1 && lane == 0)
+      role_mma<DT, D, CAUSAL>(sbase, c, tbase, p);
+  } else if (wg == 1 || wg == 2) {
+    if (static_cast<int>(wg) - 1 < C::kNQT) role_softmax<DT, D, CAUSAL>(wg - 1, c, tbase, p);
+  } else {
+    role_correction<DT, D, CAUSAL>(c, tbase, p);
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, C::kTmemCols);
+  }
+}
+
+}  // namespace wsattn

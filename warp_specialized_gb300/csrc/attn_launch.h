@@ -1,0 +1,57 @@
+// attn_launch.h - host-side glue between the C ABI (attn_api.cu) and the
+// per-dtype kernel instantiation units (inst_*.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace wsattn {
+
+// cuTensorMapEncodeTiled, resolved at run time through the runtime's
+// driver entry-point query so that the library does not link libcuda.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct LaunchArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, N, d;
+  int causal;
+  float scale_log2;   // softmax scale (with q/k descales) times log2(e)
+  float out_scale;    // v descale
+  cudaStream_t stream;
+  int device;
+  int num_sms;
+  unsigned long long timeout_ns;
+  unsigned int* status;  // device watchdog words
+  unsigned int* where;
+  EncodeTiledFn encode;
+};
+
+// status codes (identical to attn.h)
+enum : int {
+  kOk = 0,
+  kErrInvalidArg = 1,
+  kErrUnsupported = 2,
+  kErrMisaligned = 3,
+  kErrDevice = 4,
+  kErrCuda = 5,
+  kErrTimeout = 6,
+};
+
+constexpr int kMaxDevices = 64;
+
+// One entry per element type; each returns a status code.
+int launch_fp32(const LaunchArgs& a);
+int launch_fp16(const LaunchArgs& a);
+int launch_bf16(const LaunchArgs& a);
+int launch_fp8(const LaunchArgs& a);
+
+}  // namespace wsattn

@@ -1,0 +1,12 @@
+// bf16 instances: d = 64, 128, 256
+#include "attn_instance.cuh"
+namespace wsattn {
+int launch_bf16(const LaunchArgs& a) {
+  switch (a.d) {
+    case 64: return launch_mask<2, 64>(a);
+    case 128: return launch_mask<2, 128>(a);
+    case 256: return launch_mask<2, 256>(a);
+    default: return kErrUnsupported;
+  }
+}
+}  // namespace wsattn
