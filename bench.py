@@ -1,0 +1,386 @@
+"""Benchmark of the fused attention forward pass on GB300.
+
+python bench.py --gpus N --steps K --warmup W [--impl reference] [--causal]
+
+One step = one forward pass over the whole workload (bf16 B=2 H=16 N=8192
+d=128, non-causal, the long-sequence head-dim-128 setting) with Q, K, V
+already resident in HBM.  W untimed steps, then exactly K timed steps
+bracketed by a barrier and a device synchronise.  L2 is flushed (a 256 MiB
+write) before every timed step, outside the kernel's events.  The kernel
+time is measured with CUDA events on the launching stream; `value` is the
+whole-job throughput in TFLOP/s (4*B*H*N^2*d FLOPs per step, halved when
+causal), the max over ranks.  With N GPUs (torchrun, one rank per GPU) every
+rank runs its own copy of the workload (independent heads; no exchange), so
+scaling is weak.
+
+Also reported: `e2e` (the same metric through the public C-ABI call with the
+inputs copied from pinned host memory and O/LSE copied back every step),
+`roofline` (achieved TFLOP/s of the kernel against the measured dense bf16
+peak), `clocks` (nvidia-smi during the timed region) and `cpu_baseline` (the
+fp64 oracle timed on the host cores on a bounded sample of the workload).
+
+--impl reference times that oracle alone, on the same workload, metric and
+unit (each step a bounded sample of rows), and prints the same JSON line
+with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import attn_inputs as ai  # noqa: E402
+
+WORKLOAD = "bf16_n8192_d128"
+METRIC = "attention fwd TFLOPs/s on 1 GB300 (and % of dense BF16/FP8 tensor peak)"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_NAME = "attn_fwd_kernel"
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_env():
+    """(rank, local_rank, world) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The max of x over all ranks (x itself when world == 1)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(flops_per_step: float, steps: int, world: int, max_time_s: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` steps of the workload."""
+    return world * steps * flops_per_step / max_time_s / 1e12
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "warp_specialized_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the timed kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{WORKLOAD}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_digest:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_source_digest():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock, power and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period), "-i", str(self.gpu)],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.count(",") >= 8]
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import warp_specialized_gb300 as ws
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ws.load_library(build_if_missing=True)
+
+    inp = ai.workload(WORKLOAD)
+    B, H, N, d = inp.shape
+    causal = bool(args.causal)
+    flops = ai.workload_flops(B, H, N, d, causal)
+    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    qp, kp, vp, op, lp = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr()
+
+    def step():
+        rc = ws.attn_fwd_raw(qp, kp, vp, op, lp, B, H, N, d, inp.scale, causal, ws.ATTN_BF16, sh)
+        if rc != 0:
+            raise ws.AttnError(rc)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if ws.attn_fwd_status() != 0:
+        raise RuntimeError("watchdog fired during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank if world > 1 else torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    if ws.attn_fwd_status() != 0:
+        raise RuntimeError("watchdog fired during the timed region")
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_s = sum(kernel_ms) / 1e3
+    max_total_s = max_over_ranks(total_s, world, dev)
+    value = weak_scaling_value(flops, args.steps, world, max_total_s)
+    avg_ms = max_total_s / args.steps * 1e3
+    achieved = flops / (avg_ms / 1e3) / 1e12
+
+    # end to end through the public call: pinned host inputs in, O/LSE out
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
+    hq, hk, hv = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
+    ho = torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_value = None
+    if e2e_steps:
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        e2e_s = max_over_ranks(es.elapsed_time(ee) / 1e3, world, dev)
+        e2e_value = round(weak_scaling_value(flops, e2e_steps, world, e2e_s), 2)
+        if ws.attn_fwd_status() != 0:
+            raise RuntimeError("watchdog fired during the end-to-end leg")
+
+    peak, peak_src = load_peaks()
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(avg_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} (B={B} H={H} N={N} d={d}, "
+                               f"{'causal' if causal else 'non-causal'}, N(0,1) inputs)",
+                   "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                   "flops_per_step": flops,
+                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "parallelism": f"replica per GPU x{world} (independent heads, no exchange)"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps + e2e_steps,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": UNIT, "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(), "peak_source": peak_src,
+                     "kernel": KERNEL_NAME},
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result, rank, world
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sample(target_s: float, seed: int = 0):
+    """Times the fp64 oracle on seeded rows of every head of the workload,
+    sized to take about target_s seconds.  Returns (TFLOP/s, seconds, rows,
+    threads, description)."""
+    import numpy as np
+
+    import oracle
+    inp = ai.workload(WORKLOAD)
+    B, H, N, d = inp.shape
+    q, k, v = (x.numpy() for x in inp.as_float64())
+    g = np.random.default_rng(seed)
+    # calibrate on 2 rows per head
+    rows = g.choice(N, size=2, replace=False)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, inp.scale, False, rows=rows)
+    dt = time.perf_counter() - t0
+    per_row = dt / (2 * B * H)
+    n_rows = int(max(2, min(N, target_s / max(per_row, 1e-9) / (B * H))))
+    rows = g.choice(N, size=n_rows, replace=False)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, inp.scale, False, rows=rows)
+    dt = time.perf_counter() - t0
+    fl = 4.0 * N * d * n_rows * B * H
+    desc = (f"{n_rows} seeded query rows x all {B * H} heads of {WORKLOAD} "
+            f"({n_rows * B * H} rows, {fl / 1e9:.1f} GFLOP), non-causal, fp64")
+    return fl / dt / 1e12, dt, n_rows, oracle.max_threads(), desc
+
+
+def run_reference(args):
+    """The oracle alone on the host cores, same metric/unit/workload."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None, rank, world
+    per_step_target = max(0.5, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(per_step_target / 4)
+    rates, times = [], []
+    desc = ""
+    cores = 1
+    for i in range(args.steps):
+        tf, dt, n_rows, cores, desc = oracle_sample(per_step_target, seed=i + 1)
+        rates.append(tf)
+        times.append(dt)
+    value = statistics.median(rates)
+    inp_shape = ai.WORKLOADS[WORKLOAD][:4]
+    B, H, N, d = inp_shape
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.median(times) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{WORKLOAD} (B={B} H={H} N={N} d={d}, non-causal, N(0,1) "
+                               "inputs); each step a bounded row sample",
+                   "B": B, "H": H, "N": N, "d": d, "causal": False},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    return result, rank, world
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        result, rank, _ = run_reference(args)
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+        return
+
+    result, rank, world = run_gpu(args)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            tf, dt, n_rows, cores, desc = oracle_sample(args.cpu_seconds)
+            result["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores,
+                                      "kind": "oracle", "sample": desc,
+                                      "seconds": round(dt, 2)}
+        print(json.dumps(result), flush=True)
+
+
+if __name__ == "__main__":
+    main()
