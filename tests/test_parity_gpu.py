@@ -63,6 +63,17 @@ def test_persistent_loop_more_items_than_sms(causal):
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["nc", "causal"])
+def test_schedule_partial_reversed_round(causal):
+    """200 work items on a 152-CTA grid: the second round runs in reversed
+    CTA order and is only partly filled."""
+    inp = ai.make_inputs(1, 200, 256, 128, "bf16", seed=9)
+    o, lse = run_gpu(inp, causal)
+    heads = [(0, 0), (0, 151), (0, 152), (0, 199)]
+    compare(inp, causal, o, lse, heads=heads)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["nc", "causal"])
 def test_outlier_channels_small(causal):
     inp = ai.make_inputs(2, 4, 512, 64, "fp16", seed=11, outliers=4, v_dist="uniform")
     o, lse = run_gpu(inp, causal)

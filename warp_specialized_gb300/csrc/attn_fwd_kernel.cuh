@@ -53,16 +53,9 @@ namespace wsattn {
 // status codes mirrored from attn.h (kept numerically identical)
 constexpr unsigned kStatusTimeout = 6u;
 
-// element types: 0 fp32 (tf32 products), 1 fp16, 2 bf16, 3 e4m3
+// element types: 1 fp16, 2 bf16, 3 e4m3 (fp32 inputs use attn_fwd_fp32.cuh)
 template <int DT>
 struct DTypeTraits;
-template <>
-struct DTypeTraits<0> {
-  static constexpr int kEsize = 4;
-  static constexpr uint32_t kFmt = 2;  // tf32
-  static constexpr MmaKind kKind = MmaKind::kTF32;
-  static constexpr int kOutEsize = 4;
-};
 template <>
 struct DTypeTraits<1> {
   static constexpr int kEsize = 2;
@@ -175,6 +168,18 @@ __device__ __forceinline__ Item decode_item(int it, const AttnParams& p) {
   return r;
 }
 
+// Static persistent schedule: in round r, CTA c takes item r*G + c on even
+// rounds and r*G + (G-1-c) on odd rounds ("snake" order).  With the items
+// listed most-work-first (causal) this evens out the per-CTA totals, and
+// neighbouring CTAs still work on neighbouring items (the same head's K/V
+// stays hot in L2).  Returns -1 for a round with no item for this CTA.
+__device__ __forceinline__ int round_item(int r, int n_items) {
+  const int g = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  const int it = r * g + ((r & 1) ? g - 1 - c : c);
+  return it < n_items ? it : -1;
+}
+
 // Shared-memory control block (after the tiles).
 template <int NSLOT>
 struct Ctrl {
@@ -235,7 +240,9 @@ __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   uint32_t loads = 0;  // total ring loads issued
   bool ok = true;
 
-  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+  for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
+    const int it = round_item(rnd, p.n_items);
+    if (it < 0) continue;
     const Item w = decode_item<C::kNQT, CAUSAL>(it, p);
 #pragma unroll
     for (int t = 0; t < C::kNQT; ++t) {
@@ -343,7 +350,9 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
     }
   };
 
-  for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+  for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
+    const int it = round_item(rnd, p.n_items);
+    if (it < 0) continue;
     const Item w = decode_item<NQT, CAUSAL>(it, p);
     // S_t(0) for every tile
     int ks;
@@ -435,79 +444,99 @@ __device__ __forceinline__ uint32_t pack2_e4m3(float a, float b) {
   return static_cast<uint32_t>(*reinterpret_cast<uint16_t*>(&v));
 }
 
-// Exponentials of 64 scores of one row, written as P into Tensor Memory
-// (the P columns of this half: 16-bit types pack two per column, e4m3 four,
-// tf32 one).  Returns the sum of the fp32 exponentials (before rounding).
-template <int DT>
-__device__ __forceinline__ float exp_store_half(const float (&s)[64], float sl2, float neg_m,
-                                                uint32_t taddr_p) {
-  float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-  if constexpr (DT == 0) {
-    uint32_t pk[64];
-#pragma unroll
-    for (int i = 0; i < 64; i += 4) {
-      const float e0 = ex2_approx(fmaf(s[i + 0], sl2, neg_m));
-      const float e1 = ex2_approx(fmaf(s[i + 1], sl2, neg_m));
-      const float e2 = ex2_approx(fmaf(s[i + 2], sl2, neg_m));
-      const float e3 = ex2_approx(fmaf(s[i + 3], sl2, neg_m));
-      sum0 += e0;
-      sum1 += e1;
-      sum2 += e2;
-      sum3 += e3;
-      pk[i + 0] = __float_as_uint(e0);
-      pk[i + 1] = __float_as_uint(e1);
-      pk[i + 2] = __float_as_uint(e2);
-      pk[i + 3] = __float_as_uint(e3);
-    }
-    tmem_st_x64(taddr_p, pk);
-  } else if constexpr (DT == 3) {
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 64; i += 4) {
-      const float e0 = ex2_approx(fmaf(s[i + 0], sl2, neg_m));
-      const float e1 = ex2_approx(fmaf(s[i + 1], sl2, neg_m));
-      const float e2 = ex2_approx(fmaf(s[i + 2], sl2, neg_m));
-      const float e3 = ex2_approx(fmaf(s[i + 3], sl2, neg_m));
-      sum0 += e0;
-      sum1 += e1;
-      sum2 += e2;
-      sum3 += e3;
-      pk[i / 4] = pack2_e4m3(e0, e1) | (pack2_e4m3(e2, e3) << 16);
-    }
-    tmem_st_x16(taddr_p, pk);
-  } else {
-    uint32_t pk[32];
-#pragma unroll
-    for (int i = 0; i < 64; i += 4) {
-      const float e0 = ex2_approx(fmaf(s[i + 0], sl2, neg_m));
-      const float e1 = ex2_approx(fmaf(s[i + 1], sl2, neg_m));
-      const float e2 = ex2_approx(fmaf(s[i + 2], sl2, neg_m));
-      const float e3 = ex2_approx(fmaf(s[i + 3], sl2, neg_m));
-      sum0 += e0;
-      sum1 += e1;
-      sum2 += e2;
-      sum3 += e3;
-      pk[i / 2] = pack2<DT>(e0, e1);
-      pk[i / 2 + 1] = pack2<DT>(e2, e3);
-    }
-    tmem_st_x32(taddr_p, pk);
-  }
-  return (sum0 + sum1) + (sum2 + sum3);
+// Packed fp32 pairs (Blackwell f32x2 arithmetic: one instruction, two lanes
+// of work).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
-// Loads 64 scores (columns col0 .. col0+63 of the row) and applies the mask:
-// key columns at or past `lim` become -inf.
-__device__ __forceinline__ void load_scores_half(uint32_t taddr, int col0, int lim,
-                                                 float (&s)[64]) {
-  uint32_t raw[64];
-  tmem_ld_x64(taddr + col0, raw);
+// Largest of the 128 scores of a row: four independent three-input max
+// chains of 32 scores each.
+__device__ __forceinline__ float max128(const float (&s)[128]) {
+  float m[4];
 #pragma unroll
-  for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(raw[i]);
-  if (lim < col0 + 64) {
+  for (int k = 0; k < 4; ++k) {
+    const float* x = s + 32 * k;
+    float a = max3f(x[0], x[1], x[2]);
 #pragma unroll
-    for (int i = 0; i < 64; ++i) s[i] = (col0 + i < lim) ? s[i] : -INFINITY;
+    for (int i = 3; i < 31; i += 2) a = max3f(a, x[i], x[i + 1]);
+    m[k] = fmaxf(a, x[31]);
   }
+  return fmaxf(max3f(m[0], m[1], m[2]), m[3]);
 }
+
+// Exponentials of scores OFF .. OFF+63 of one row, written as P into Tensor
+// Memory at taddr_p (16-bit types pack two per column, e4m3 four).
+// x = s * scale_log2 - m in packed pairs, p = 2^x on MUFU.  Returns the sum
+// of the fp32 exponentials (before rounding to the P type).
+template <int DT, int OFF>
+__device__ __forceinline__ float exp_store_half(const float (&s)[128], float sl2, float neg_m,
+                                                uint32_t taddr_p) {
+  const uint64_t k2 = f2_pack(sl2, sl2);
+  const uint64_t b2 = f2_pack(neg_m, neg_m);
+  uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+  constexpr int kWords = DT == 3 ? 16 : 32;
+  uint32_t pk[kWords];
+#pragma unroll
+  for (int ii = 0; ii < 64; ii += 4) {
+    const int i = OFF + ii;
+    float x0, x1, x2, x3;
+    f2_unpack(f2_fma(f2_pack(s[i], s[i + 1]), k2, b2), x0, x1);
+    f2_unpack(f2_fma(f2_pack(s[i + 2], s[i + 3]), k2, b2), x2, x3);
+    const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+    const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
+    acc0 = f2_add(acc0, f2_pack(e0, e1));
+    acc1 = f2_add(acc1, f2_pack(e2, e3));
+    if constexpr (DT == 3) {
+      pk[ii / 4] = pack2_e4m3(e0, e1) | (pack2_e4m3(e2, e3) << 16);
+    } else {
+      pk[ii / 2] = pack2<DT>(e0, e1);
+      pk[ii / 2 + 1] = pack2<DT>(e2, e3);
+    }
+  }
+  if constexpr (DT == 3)
+    tmem_st_x16(taddr_p, pk);
+  else
+    tmem_st_x32(taddr_p, pk);
+  float a0, a1;
+  f2_unpack(f2_add(acc0, acc1), a0, a1);
+  return a0 + a1;
+}
+
+// The subtraction reference moves when a block's max exceeds it by more
+// than kRescaleLog2 (base-2 units of the scaled scores); otherwise alpha = 1
+// and the correction warpgroup skips the O rescale.  A threshold t > 0 lets
+// probabilities reach 2^t: O / l and m + log2 l are unchanged in real
+// arithmetic, but the largest probability of a row is then no longer exactly
+// 1 and picks up the P type's rounding (2^-8 relative in bf16), which a
+// peaked softmax passes straight into O.  The exact running max (0) keeps
+// that term exact.
+constexpr float kRescaleLog2 = 0.0f;
 
 template <int DT, int D, bool CAUSAL>
 __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
@@ -522,12 +551,16 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
   uint32_t s_waits = 0;
   uint32_t iter = 0;
 
-  for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++iter) {
+  for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items; ++rnd) {
+    const int it = round_item(rnd, p.n_items);
+    if (it < 0) continue;
     const Item w = decode_item<C::kNQT, CAUSAL>(it, p);
     const int qt = w.qt0 + t;
     const int n = w.n[t];
-    float m_run = -INFINITY;
+    float m_run = -INFINITY;  // subtraction reference (log2 units)
     float l_run = 0.f;
+    float* const inv_l_dst = &c->inv_l[iter & 1u][t][r];
+    float* const alpha_dst = &c->alpha[t][r];
     for (int j = 0; j < n; ++j) {
       if (!wait_bar(smem_u32(&c->s_full[t]), s_waits & 1u, wc, 0x21)) return;
       ++s_waits;
@@ -537,51 +570,51 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
       int lim = p.N - j * kBlock;
       if (CAUSAL && j == qt) lim = min(lim, r + 1);
 
-      // Row max over the 128 scores, reading the upper half first so that
-      // the lower half is the one left in registers (a row of 128 fp32
-      // scores does not fit the 128-register budget of a 512-thread block
-      // together with its probabilities).
-      float s[64];
-      load_scores_half(taddr, 64, lim, s);
-      float mx = s[0];
+      // The whole row of scores in registers (the softmax warpgroups run
+      // with 168 registers per thread).
+      float s[kBlock];
+      {
+        uint32_t raw[kBlock];
+        tmem_ld_2x64(taddr, raw);
 #pragma unroll
-      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, s[i]);
-      load_scores_half(taddr, 0, lim, s);
+        for (int i = 0; i < kBlock; ++i) s[i] = __uint_as_float(raw[i]);
+      }
+      if (lim < kBlock) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) mx = fmaxf(mx, s[i]);
+        for (int i = 0; i < kBlock; ++i) s[i] = i < lim ? s[i] : -INFINITY;
+      }
+      const float mx = max128(s) * sl2;
 
-      const float m_new = fmaxf(m_run, mx * sl2);
+      float alpha = 1.0f;
+      if (mx > m_run + kRescaleLog2) {
+        alpha = ex2_approx(m_run - mx);  // 0 on the first block (m_run = -inf)
+        m_run = mx;
+      }
       // subtraction reference: 0 while every key so far is masked
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      // rescale factor; exactly 1 when the max did not move, 0 on the
-      // first block (m_run = -inf)
-      const float alpha = m_run == m_use ? 1.0f : ex2_approx(m_run - m_use);
-      c->alpha[t][r] = alpha;
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      *alpha_dst = alpha;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c->sc_full[t]));
 
-      // P over the first kPCols columns of S: the lower half's P lands on
-      // columns already read into registers, the upper half is re-read
-      // before its P overwrites anything it still needs.
+      // P over the first kPCols columns of S (already in registers)
       const float neg_m = -m_use;
-      float sum = exp_store_half<DT>(s, sl2, neg_m, taddr);
-      load_scores_half(taddr, 64, lim, s);
-      sum += exp_store_half<DT>(s, sl2, neg_m, taddr + C::kPCols / 2);
+      const float sum = exp_store_half<DT, 0>(s, sl2, neg_m, taddr) +
+                        exp_store_half<DT, 64>(s, sl2, neg_m, taddr + C::kPCols / 2);
       l_run = alpha * l_run + sum;
-      m_run = m_new;
       tmem_st_wait();
-      if (j == n - 1) {
-        // hand 1/l to the epilogue; write LSE (natural log) for real rows
-        c->inv_l[iter & 1u][t][r] = 1.0f / l_run;
-        const int row = qt * kBlock + r;
-        if (row < p.N)
-          p.lse[static_cast<size_t>(w.bh) * p.N + row] =
-              (m_use + log2f(l_run)) * 0.6931471805599453f;
-      }
+      // hand 1/l to the epilogue before the last P is announced
+      if (j == n - 1) *inv_l_dst = __frcp_rn(l_run);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t]));
     }
+    // LSE (natural log) of the real rows
+    const int row = qt * kBlock + r;
+    if (row < p.N) {
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      p.lse[static_cast<size_t>(w.bh) * p.N + row] = (m_use + __log2f(l_run)) * 0.6931471805599453f;
+    }
+    ++iter;
   }
 }
 
@@ -591,14 +624,6 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
 template <int DT>
 __device__ __forceinline__ void store_out_chunk(void* dst, const float* v);  // 32 values
 
-template <>
-__device__ __forceinline__ void store_out_chunk<0>(void* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    d[i] = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
-                      __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
-}
 template <>
 __device__ __forceinline__ void store_out_chunk<1>(void* dst, const float* v) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -632,7 +657,9 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, con
   uint32_t sc_waits[2] = {0, 0}, o_waits[2] = {0, 0};
   uint32_t iter = 0;
 
-  for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++iter) {
+  for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items; ++rnd) {
+    const int it = round_item(rnd, p.n_items);
+    if (it < 0) continue;
     const Item w = decode_item<NQT, CAUSAL>(it, p);
     for (int j = 0; j < w.nmax; ++j) {
       for (int t = 0; t < NQT; ++t) {
@@ -653,8 +680,15 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, con
             for (int cc = 0; cc < D; cc += 32) {
               uint32_t v[32];
               tmem_ld_x32(ta + cc, v);
+              const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              for (int i = 0; i < 32; i += 2) {
+                float x0, x1;
+                f2_unpack(f2_mul(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), a2),
+                          x0, x1);
+                v[i] = __float_as_uint(x0);
+                v[i + 1] = __float_as_uint(x1);
+              }
               tmem_st_x32(ta + cc, v);
             }
             tmem_st_wait();
@@ -685,6 +719,7 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, con
         if (row < p.N) store_out_chunk<DT>(orow + cc * C::T::kOutEsize, x);
       }
     }
+    ++iter;
   }
 }
 
@@ -738,18 +773,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tbase = c->tmem_base;
 
-  // Role dispatch by warpgroup.  Every thread keeps the launch's 128
-  // registers: ptxas allocates the whole kernel within the launch bound,
-  // so a setmaxnreg split would not give the softmax more to work with.
+  // Role dispatch by warpgroup, with the register file split among them:
+  // 88 (producer / MMA) + 168 + 168 (softmax) + 80 (correction) = 504 of
+  // the 4 * 128 registers per thread the block is launched with (the host
+  // refuses to launch a build with any other count).
   const uint32_t wg = warp >> 2;
   if (wg == 0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
     if (warp == 0 && lane == 0)
       role_producer<DT, D, CAUSAL>(&tmQ, &tmK, &tmV, sbase, c, p);
     else if (warp == 1 && lane == 0)
       role_mma<DT, D, CAUSAL>(sbase, c, tbase, p);
   } else if (wg == 1 || wg == 2) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;");
     if (static_cast<int>(wg) - 1 < C::kNQT) role_softmax<DT, D, CAUSAL>(wg - 1, c, tbase, p);
   } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
     role_correction<DT, D, CAUSAL>(c, tbase, p);
   }
 

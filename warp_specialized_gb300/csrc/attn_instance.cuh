@@ -41,8 +41,10 @@ template <int DT, int D, bool CAUSAL>
 int launch_instance(const LaunchArgs& a) {
   using C = Cfg<DT, D>;
   auto kern = attn_fwd_kernel<DT, D, CAUSAL>;
-  // Per device, once: opt in to the shared memory size and check that the
-  // kernel fits the launch (512 threads, at most 128 registers each).
+  // Per device, once: opt in to the shared memory size, and refuse to run
+  // unless the kernel is launched with exactly 128 registers per thread:
+  // the warpgroups' setmaxnreg split (88 + 168 + 168 + 80) draws on that
+  // pool and could never be satisfied by a smaller one.
   static std::atomic<int> ready[kMaxDevices];
   if (a.device < 0 || a.device >= kMaxDevices) return kErrDevice;
   int st = ready[a.device].load(std::memory_order_acquire);
@@ -57,7 +59,7 @@ int launch_instance(const LaunchArgs& a) {
       cudaGetLastError();
       return kErrCuda;
     }
-    st = (fa.numRegs <= 128 && fa.maxThreadsPerBlock >= kThreads) ? 1 : 2;
+    st = (fa.numRegs == 128 && fa.maxThreadsPerBlock >= kThreads) ? 1 : 2;
     ready[a.device].store(st, std::memory_order_release);
   }
   if (st != 1) return kErrUnsupported;
