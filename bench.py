@@ -226,34 +226,66 @@ def run_gpu(args):
     avg_ms = max_total_s / args.steps * 1e3
     achieved = flops / (avg_ms / 1e3) / 1e12
 
-    # end to end through the public call: pinned host inputs in, O/LSE out
-    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
+    # End to end through the public call: every step copies its inputs from
+    # pinned host memory, runs the forward pass and copies O and LSE back.
+    # Steps are independent, so they are pipelined the way a serving loop
+    # would run them: two device buffer sets, the input copies of step i+1
+    # (one stream) overlap the kernel of step i (a second stream) and the
+    # output copies of step i-1 (a third), ordered by events.
+    e2e_steps = 0 if args.no_e2e else max(2, min(args.steps, 20))
     hq, hk, hv = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
-    ho = torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
-    hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    ho = [torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    hl = [torch.empty((B, H, N), dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        step()
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-
+    d2h = ho[0].numel() * ho[0].element_size() + hl[0].numel() * hl[0].element_size()
     e2e_value = None
     if e2e_steps:
-        e2e_step()
+        bufs = [dict(q=q, k=k, v=v, o=o, l=lse)]
+        bufs.append(dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v),
+                         o=torch.empty_like(o), l=torch.empty_like(lse)))
+        s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_run = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        for b in range(2):  # mark every buffer free
+            ev_run[b].record(s_run)
+            ev_out[b].record(s_out)
+
+        def e2e_step(i):
+            b = i & 1
+            bb = bufs[b]
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_run[b])          # the kernel of step i-2 has read them
+                bb["q"].copy_(hq, non_blocking=True)
+                bb["k"].copy_(hk, non_blocking=True)
+                bb["v"].copy_(hv, non_blocking=True)
+                ev_in[b].record(s_in)
+            s_run.wait_event(ev_in[b])
+            s_run.wait_event(ev_out[b])             # O / LSE of step i-2 are copied out
+            rc = ws.attn_fwd_raw(bb["q"].data_ptr(), bb["k"].data_ptr(), bb["v"].data_ptr(),
+                                 bb["o"].data_ptr(), bb["l"].data_ptr(), B, H, N, d, inp.scale,
+                                 causal, ws.ATTN_BF16, s_run.cuda_stream)
+            if rc != 0:
+                raise ws.AttnError(rc)
+            ev_run[b].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_run[b])
+                ho[b].copy_(bb["o"], non_blocking=True)
+                hl[b].copy_(bb["l"], non_blocking=True)
+                ev_out[b].record(s_out)
+
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        es.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        ee.record(stream)
+        es.record(s_in)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        s_out.wait_event(ev_out[(e2e_steps - 1) & 1])
+        ee.record(s_out)
         torch.cuda.synchronize()
         e2e_s = max_over_ranks(es.elapsed_time(ee) / 1e3, world, dev)
         e2e_value = round(weak_scaling_value(flops, e2e_steps, world, e2e_s), 2)
@@ -273,7 +305,8 @@ def run_gpu(args):
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "parallelism": f"replica per GPU x{world} (independent heads, no exchange)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "schedule": "steps pipelined over two buffer sets: H2D(i+1) || kernel(i) || D2H(i-1)"},
         "gpu_launches": args.steps + e2e_steps,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": UNIT, "frac": round(achieved / peak, 4),
@@ -301,12 +334,13 @@ def oracle_sample(target_s: float, seed: int = 0):
     B, H, N, d = inp.shape
     q, k, v = (x.numpy() for x in inp.as_float64())
     g = np.random.default_rng(seed)
-    # calibrate on 2 rows per head
-    rows = g.choice(N, size=2, replace=False)
+    # warm the thread pool, then calibrate on 8 rows per head
+    oracle.attn_fwd(q, k, v, inp.scale, False, rows=g.choice(N, size=1, replace=False))
+    rows = g.choice(N, size=8, replace=False)
     t0 = time.perf_counter()
     oracle.attn_fwd(q, k, v, inp.scale, False, rows=rows)
     dt = time.perf_counter() - t0
-    per_row = dt / (2 * B * H)
+    per_row = dt / (8 * B * H)
     n_rows = int(max(2, min(N, target_s / max(per_row, 1e-9) / (B * H))))
     rows = g.choice(N, size=n_rows, replace=False)
     t0 = time.perf_counter()
@@ -337,7 +371,7 @@ def run_reference(args):
     inp_shape = ai.WORKLOADS[WORKLOAD][:4]
     B, H, N, d = inp_shape
     result = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": statistics.median(times) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
