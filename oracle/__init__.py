@@ -58,6 +58,9 @@ def _load():
                                                       i64, ctypes.c_double, ctypes.c_int,
                                                       i64]
             lib.oracle_attn_fwd_blockwise.restype = ctypes.c_int
+            lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64,
+                                            ctypes.c_double, ctypes.c_int, ctypes.c_int]
+            lib.oracle_attn_bwd.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -118,3 +121,19 @@ def attn_fwd_blockwise(q, k, v, scale: float, causal: bool, block: int):
     if rc != 0:
         raise ValueError("oracle_attn_fwd_blockwise rejected its arguments")
     return o, lse
+
+
+def attn_bwd(q, k, v, dout, scale: float, causal: bool, n_threads: int = 0):
+    """Gradients (dQ, dK, dV) of the forward pass for the output gradient
+    dout, every row, fp64.  Shapes [B, H, N, d]."""
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    if q.ndim != 4 or any(x.shape != q.shape for x in (k, v, dout)):
+        raise ValueError("q, k, v, dout must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    dq, dk, dv = (np.empty_like(q) for _ in range(3))
+    rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                                 int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd rejected its arguments")
+    return dq, dk, dv

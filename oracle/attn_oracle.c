@@ -218,3 +218,102 @@ int oracle_attn_fwd_blockwise(const double* q, const double* k, const double* v,
     free(out);
     return 0;
 }
+
+/*
+ * Backward pass of the same function, fp64, per (b, h) (test infrastructure
+ * only, like the rest of this file).  For the loss gradient dO = dL/dO the
+ * gradients follow from differentiating the definition above:
+ *
+ *   P_ij  = exp(s_ij - LSE_i)                  (0 where masked)
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   D_i   = sum_j P_ij dP_ij                   (= dO_i . O_i)
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale * sum_j dS_ij k_j
+ *   dK_j  = scale * sum_i dS_ij q_i
+ *
+ * The logsumexp output of the forward is what makes this computable block
+ * by block without the running max ("Warp specialization" concept card,
+ * section "Implementation sketch": the consumer returns row_max +
+ * log(row_sum) next to the output).  Here every score row is materialised
+ * and LSE is recomputed exactly.  Arrays are [B, H, N, d]; all of dq, dk,
+ * dv are written.  Returns 0, or -1 on bad arguments / allocation failure.
+ */
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    double* dq, double* dk, double* dv,
+                    int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                    int n_threads) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 1 || H < 1 || N < 1 || d < 1)
+        return -1;
+    int failed = 0;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        const double* qh = q + bh * N * d;
+        const double* kh = k + bh * N * d;
+        const double* vh = v + bh * N * d;
+        const double* doh = dout + bh * N * d;
+        double* dqh = dq + bh * N * d;
+        double* dkh = dk + bh * N * d;
+        double* dvh = dv + bh * N * d;
+        double* prow = (double*)malloc((size_t)N * sizeof(double));
+        double* dprow = (double*)malloc((size_t)N * sizeof(double));
+        if (!prow || !dprow) {
+            free(prow);
+            free(dprow);
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+            continue;
+        }
+        for (int64_t x = 0; x < N * d; ++x) {
+            dqh[x] = 0.0;
+            dkh[x] = 0.0;
+            dvh[x] = 0.0;
+        }
+        for (int64_t i = 0; i < N; ++i) {
+            /* scores, max, LSE of row i */
+            double m = -INFINITY;
+            for (int64_t j = 0; j < N; ++j) {
+                if (causal && j > i) {
+                    prow[j] = -INFINITY;
+                    continue;
+                }
+                double acc = 0.0;
+                for (int64_t c = 0; c < d; ++c) acc += qh[i * d + c] * kh[j * d + c];
+                prow[j] = scale * acc;
+                if (prow[j] > m) m = prow[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < N; ++j) l += exp(prow[j] - m);
+            double lse = m + log(l);
+            /* P, dP, D */
+            double D = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                prow[j] = exp(prow[j] - lse);
+                double acc = 0.0;
+                for (int64_t c = 0; c < d; ++c) acc += doh[i * d + c] * vh[j * d + c];
+                dprow[j] = acc;
+                D += prow[j] * acc;
+            }
+            /* accumulate the three gradients */
+            for (int64_t j = 0; j < N; ++j) {
+                double pij = prow[j];
+                if (pij == 0.0) continue;
+                double ds = pij * (dprow[j] - D);
+                for (int64_t c = 0; c < d; ++c) {
+                    dvh[j * d + c] += pij * doh[i * d + c];
+                    dqh[i * d + c] += scale * ds * kh[j * d + c];
+                    dkh[j * d + c] += scale * ds * qh[i * d + c];
+                }
+            }
+        }
+        free(prow);
+        free(dprow);
+    }
+    (void)n_threads;
+    return failed ? -1 : 0;
+}
