@@ -83,11 +83,16 @@ def load_peaks():
         return FALLBACK_BF16_TFLOPS, "fallback (no MEASURED_PEAKS.json)"
 
 
+# The sources the timed forward kernel is built from (a change to any of
+# them invalidates the profiled traffic figure).
+KERNEL_SOURCES = ("ptx_sm103.cuh", "attn_fwd_kernel.cuh", "attn_instance.cuh", "inst_bf16.cu")
+
+
 def kernel_source_digest() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "warp_specialized_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]

@@ -1,6 +1,6 @@
 /*
- * attn.h - C ABI of the GB300 (sm_103a) fused attention forward library
- * (libattn_sm103.so).
+ * attn.h - C ABI of the GB300 (sm_103a) fused attention library
+ * (libattn_sm103.so): the forward pass, and its backward pass (attn_bwd).
  *
  * The operation (one call = one whole forward pass over every (b, h)):
  *
@@ -54,7 +54,7 @@ extern "C" {
 struct CUstream_st;
 
 typedef enum {
-    ATTN_FP32 = 0,      /* fp32 in, fp32 out; the matrix products run in tf32 */
+    ATTN_FP32 = 0,      /* fp32 in, fp32 out, exact fp32 arithmetic (CUDA cores) */
     ATTN_FP16 = 1,      /* fp16 in, fp16 out, fp32 accumulation */
     ATTN_BF16 = 2,      /* bf16 in, bf16 out, fp32 accumulation */
     ATTN_FP8_E4M3 = 3   /* e4m3 in (descales 1.0 through attn_fwd), bf16 out */
@@ -114,6 +114,46 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
  * the synchronisation itself reports an error.
  */
 int attn_fwd_status(struct CUstream_st* stream);
+
+/*
+ * attn_bwd_workspace_size - bytes of device workspace attn_bwd needs for
+ * this shape: 8 bytes per query row, rows rounded up to whole 128-row tiles
+ * per head (B * H * ceil(N / 128) * 128 * 8).  0 if a size is < 1.
+ */
+unsigned long long attn_bwd_workspace_size(int B, int H, int N);
+
+/*
+ * attn_bwd - backward pass: the gradients of the forward pass of attn_fwd
+ * for an output gradient dO, using the forward's O and LSE:
+ *     P_ij  = exp(scale q_i.k_j - LSE_i)   (0 where masked)
+ *     D_i   = dO_i . O_i
+ *     dS_ij = P_ij (dO_i . v_j - D_i)
+ *     dV_j  = sum_i P_ij dO_i
+ *     dQ_i  = scale sum_j dS_ij k_j
+ *     dK_j  = scale sum_i dS_ij q_i
+ * The LSE the forward returns (natural log, "Warp specialization" concept
+ * card, section "Implementation sketch": row_max + log(row_sum)) is what
+ * lets each block recompute its probabilities without a running max.
+ *   q, k, v, o, dout : [B, H, N, d] device tensors of `dtype`, 16-byte aligned
+ *                      (o and lse as returned by attn_fwd for these q, k, v,
+ *                      scale and causal).
+ *   lse              : [B, H, N] fp32, 4-byte aligned.
+ *   dq, dk, dv       : [B, H, N, d] device outputs of `dtype`, 16-byte
+ *                      aligned, every element written once.
+ *   workspace        : device scratch of at least attn_bwd_workspace_size()
+ *                      bytes, 16-byte aligned, owned by the caller; its
+ *                      contents on entry do not matter and on return are
+ *                      unspecified.  Calls that share a workspace must not
+ *                      overlap on the device.
+ *   dtype            : ATTN_FP16 or ATTN_BF16; d : 64 or 128; other
+ *                      arguments as attn_fwd.
+ * Three kernels are enqueued on `stream`.  Errors as attn_fwd, plus
+ * ATTN_ERR_INVALID_ARG for a workspace that is missing or too small.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, void* workspace,
+             unsigned long long workspace_bytes, int B, int H, int N, int d, float scale,
+             int causal, int dtype, struct CUstream_st* stream);
 
 /* attn_status_string - a static, human-readable name for a status code. */
 const char* attn_status_string(int status);

@@ -20,7 +20,8 @@ def lib():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+|unsigned\s+|long\s+)*\w+\s*\*?\s*(attn_\w+)\s*\(",
+                                 text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -86,3 +87,27 @@ def test_no_device_is_reported():
     lib = ws.load_library(build_if_missing=True)
     assert _call(lib) == 4
     assert lib.attn_fwd_status(None) == 4
+
+
+def test_bwd_workspace_size(lib):
+    assert lib.attn_bwd_workspace_size(2, 3, 200) == 2 * 3 * 256 * 8
+    assert lib.attn_bwd_workspace_size(1, 1, 128) == 128 * 8
+    assert lib.attn_bwd_workspace_size(0, 1, 128) == 0
+
+
+def _bwd(lib, q=A, k=A, v=A, o=A, do=A, lse=A, dq=A, dk=A, dv=A, ws=A, wsb=1 << 20, B=1, H=1,
+         N=128, d=128, scale=0.1, causal=0, dtype=2):
+    return lib.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, wsb, B, H, N, d, scale, causal,
+                        dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"o": 0}, 1), ({"do": 0}, 1), ({"dq": 0}, 1), ({"dk": 0}, 1), ({"dv": 0}, 1), ({"ws": 0}, 1),
+    ({"q": 0}, 1), ({"lse": 0}, 1), ({"N": 0}, 1), ({"scale": 0.0}, 1), ({"causal": 3}, 1),
+    ({"wsb": 128 * 8 - 1}, 1), ({"dtype": 0}, 2), ({"dtype": 3}, 2), ({"dtype": 7}, 1),
+    ({"d": 256}, 2), ({"d": 96}, 2),
+    ({"o": A + 8}, 3), ({"do": A + 2}, 3), ({"dk": A + 4}, 3), ({"dv": A + 1}, 3),
+    ({"ws": A + 8}, 3), ({"dq": A + 8}, 3),
+])
+def test_bwd_bad_arguments_are_rejected(lib, kw, code):
+    assert _bwd(lib, **kw) == code

@@ -16,7 +16,8 @@ import threading
 __all__ = [
     "ATTN_FP32", "ATTN_FP16", "ATTN_BF16", "ATTN_FP8_E4M3", "AttnError", "lib_path",
     "load_library", "attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
-    "attn_watchdog_selftest", "attn_fwd_raw", "EXPORTED_SYMBOLS",
+    "attn_watchdog_selftest", "attn_fwd_raw", "attn_bwd", "attn_bwd_workspace_size",
+    "EXPORTED_SYMBOLS",
 ]
 
 ATTN_FP32, ATTN_FP16, ATTN_BF16, ATTN_FP8_E4M3 = 0, 1, 2, 3
@@ -27,7 +28,7 @@ STATUS_NAMES = {
 }
 
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
-                    "attn_watchdog_selftest")
+                    "attn_watchdog_selftest", "attn_bwd", "attn_bwd_workspace_size")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -70,6 +71,12 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_watchdog_selftest.argtypes = [ctypes.c_uint, vp]
         lib.attn_watchdog_selftest.restype = i
+        u64 = ctypes.c_ulonglong
+        lib.attn_bwd_workspace_size.argtypes = [i, i, i]
+        lib.attn_bwd_workspace_size.restype = u64
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i, i, i, i, f, i, i,
+                                 vp]
+        lib.attn_bwd.restype = i
         _lib = lib
         return lib
 
@@ -169,3 +176,41 @@ def attn_watchdog_selftest(timeout_us: int = 2000, stream=None) -> int:
     """Run the watchdog self-test kernel; returns ATTN_ERR_TIMEOUT (6) when the
     bounded wait works."""
     return int(load_library().attn_watchdog_selftest(int(timeout_us), _stream_handle(stream)))
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int) -> int:
+    """Bytes of device workspace attn_bwd needs for this shape."""
+    return int(load_library().attn_bwd_workspace_size(int(B), int(H), int(N)))
+
+
+def attn_bwd(q, k, v, o, lse, dout, scale=None, causal: bool = False, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """dQ, dK, dV of the forward pass for the output gradient dout.
+
+    q, k, v, o, dout: [B, H, N, d] fp16/bf16 CUDA tensors (o, lse from
+    attn_fwd with the same scale and mask); lse: [B, H, N] fp32.  Outputs
+    and the uint8 workspace are allocated with torch when not given.
+    Asynchronous on `stream`.  Returns (dq, dk, dv)."""
+    import torch
+    _check_qkv(q, k, v)
+    for t in (o, dout):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("o and dout must match q")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    code = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = attn_bwd_workspace_size(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = load_library().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), B, H, N, d,
+                                 float(scale), int(bool(causal)), code, _stream_handle(stream))
+    if st != 0:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv

@@ -154,6 +154,55 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   }
 }
 
+int run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+            const float* lse, void* dq, void* dk, void* dv, void* workspace,
+            unsigned long long workspace_bytes, int B, int H, int N, int d, float scale,
+            int causal, int dtype, cudaStream_t stream) {
+  if (!o || !dout || !dq || !dk || !dv || !workspace) return kErrInvalidArg;
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16) {
+    if (dtype < ATTN_FP32 || dtype > ATTN_FP8_E4M3) return kErrInvalidArg;
+    return kErrUnsupported;
+  }
+  // the forward's checks cover q, k, v, lse, sizes, scale, causal, dtype
+  int rc = check_args(q, k, v, dq, lse, B, H, N, d, scale, causal, dtype);
+  if (rc != kOk) return rc;
+  if (d != 64 && d != 128) return kErrUnsupported;
+  if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(workspace, 16))
+    return kErrMisaligned;
+  if (workspace_bytes < bwd_workspace_bytes(B, H, N)) return kErrInvalidArg;
+  int dev = -1;
+  rc = current_device(&dev);
+  if (rc != kOk) return rc;
+  if (!resolve_encode()) return kErrCuda;
+  BwdLaunchArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.workspace = workspace;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.dtype = dtype;
+  a.scale = scale;
+  a.stream = stream;
+  a.device = dev;
+  a.num_sms = g_dev[dev].num_sms;
+  a.timeout_ns = kTimeoutNs;
+  a.status = g_dev[dev].status;
+  a.where = g_dev[dev].where;
+  a.encode = g_encode;
+  return launch_bwd(a);
+}
+
 // Waits on an mbarrier that nobody arrives on, so the bounded wait runs out.
 __global__ void watchdog_selftest_kernel(unsigned long long limit_ns, unsigned int* status,
                                          unsigned int* where) {
@@ -198,6 +247,19 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
                  float v_descale, struct CUstream_st* stream) {
   return wsattn::run(q, k, v, o, lse, B, H, N, d, scale, causal, ATTN_FP8_E4M3, q_descale,
                      k_descale, v_descale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+unsigned long long attn_bwd_workspace_size(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0ull;
+  return wsattn::bwd_workspace_bytes(B, H, N);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, void* workspace,
+             unsigned long long workspace_bytes, int B, int H, int N, int d, float scale,
+             int causal, int dtype, struct CUstream_st* stream) {
+  return wsattn::run_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N,
+                         d, scale, causal, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_fwd_status(struct CUstream_st* stream) {

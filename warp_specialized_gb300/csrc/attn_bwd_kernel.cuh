@@ -1,0 +1,749 @@
+// attn_bwd_kernel.cuh - backward pass of the fused attention for sm_103a:
+// dQ, dK, dV from Q, K, V, O, dO and the forward's per-row logsumexp.
+//
+// The gradients of O = softmax(scale Q K^T [+ mask]) V for an output
+// gradient dO, per (b, h):
+//   P_ij  = exp(scale q_i.k_j - LSE_i)      (0 where masked)
+//   D_i   = dO_i . O_i                      (= sum_j P_ij dP_ij)
+//   dP_ij = dO_i . v_j
+//   dS_ij = P_ij (dP_ij - D_i)
+//   dV_j  = sum_i P_ij dO_i
+//   dQ_i  = scale sum_j dS_ij k_j
+//   dK_j  = scale sum_i dS_ij q_i
+// The forward's LSE output ("Warp specialization" concept card, section
+// "Implementation sketch": the consumer returns row_max + log(row_sum))
+// lets every block recompute its probabilities directly, without a running
+// max.
+//
+// Three kernels, all on the tensor cores where the work is a contraction:
+//   preprocess   D_i and LSE_i * log2(e) per row into a workspace padded to
+//                whole 128-row tiles (padding rows: LSE = +inf, D = 0, so
+//                their probabilities are exactly 0);
+//   dQ kernel    one 128-row query tile per work item, K_j / V_j streamed
+//                through a TMA ring: S = Q K_j^T and dP = dO V_j^T into
+//                Tensor Memory, dS written back to its own TMEM columns,
+//                dQ += dS K_j accumulated in TMEM;
+//   dK/dV kernel one 128-key tile per work item, Q_i / dO_i (and the
+//                workspace rows of tile i) streamed: S^T = K Q_i^T and
+//                dP^T = V dO_i^T, P^T and dS^T written over them in TMEM,
+//                dV += P^T dO_i and dK += dS^T Q_i accumulated in TMEM.
+// Neither kernel needs atomics; each output element is written once.
+// Roles per CTA (256 threads): warp 0 lane 0 TMA producer, warp 1 lane 0
+// MMA issuer, warps 4-7 the elementwise warpgroup (one thread per row /
+// TMEM lane) that also writes the outputs.  Every wait is bounded.
+#pragma once
+
+#include <type_traits>
+
+#include "attn_fwd_kernel.cuh"
+
+namespace wsattn {
+
+constexpr int kBwdThreads = 256;
+
+// The same bounded wait executed by a whole warp, its result made
+// warp-uniform (false for every lane if any lane gave up), for warps that
+// go on to warp-synchronous TMEM loads and stores.
+__device__ __forceinline__ bool wait_bar_all(uint32_t bar, uint32_t parity, const WaitCtx& wc,
+                                            unsigned where) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, wc, where)) != 0;
+}
+
+template <int DT, int D>
+struct BwdCfg {
+  using C = Cfg<DT, D>;
+  static constexpr int kTileBytes = C::kTileBytes;
+  static constexpr int kVecBytes = 2 * kBlock * 4;  // (lse2, D) of one 128-row tile
+  // dQ kernel: Q + dO resident, K/V ring
+  static constexpr int kMiscDq = 1024 + 512;
+  static constexpr int kSlotsDqFit = (kSmemLimit - kMiscDq - 2 * kTileBytes) / kTileBytes;
+  static constexpr int kSlotsDq = kSlotsDqFit > kMaxSlots ? kMaxSlots : kSlotsDqFit;
+  static constexpr int kSmemDq = kMiscDq + (2 + kSlotsDq) * kTileBytes;
+  // dK/dV kernel: K + V resident, ring of (Q_i, dO_i, vec_i)
+  static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;
+  static constexpr int kMiscDkv = 1024 + 512;
+  static constexpr int kStagesFit = (kSmemLimit - kMiscDkv - 2 * kTileBytes) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 4 ? 4 : kStagesFit;
+  static constexpr int kSmemDkv = kMiscDkv + 2 * kTileBytes + kStages * kStageBytes;
+  static_assert(kSlotsDq >= 2 && kStages >= 2, "backward shared-memory budget");
+  static_assert(kSmemDq <= kSmemLimit && kSmemDkv <= kSmemLimit, "shared memory budget");
+
+  // instruction descriptors: K-major x K-major (S, dP, S^T, dP^T) and
+  // TMEM A x MN-major B (dQ, dV, dK)
+  static constexpr uint32_t kIdescSS = make_idesc(C::T::kFmt, C::T::kFmt, false, kBlock, kBlock);
+  static constexpr uint32_t kIdescTS = make_idesc(C::T::kFmt, C::T::kFmt, true, D, kBlock);
+  // TMEM columns, dQ kernel: S | dP | dS (16-bit, 64 columns) | dQ
+  static constexpr uint32_t kDqS = 0, kDqDP = 128, kDqDS = 256, kDqAcc = 320;
+  // TMEM columns, dK/dV kernel: S^T (P^T over it) | dP^T (dS^T over it) | dV | dK
+  static constexpr uint32_t kKvS = 0, kKvDP = 128, kKvDV = 256, kKvDK = 256 + D;
+  static_assert(kDqAcc + D <= 512 && kKvDK + D <= 512, "Tensor Memory budget");
+};
+
+struct BwdParams {
+  const void* o;       // forward output [B, H, N, d]
+  const void* dout;    // output gradient [B, H, N, d]
+  const float* lse;    // [B, H, N]
+  float* ws;           // [B*H, Np, 2] (lse2, D), Np = N rounded up to 128
+  void* dq;
+  void* dk;
+  void* dv;
+  int N;
+  int Np;
+  int BH;
+  int nt;              // 128-row tiles per head
+  int n_items;         // BH * nt
+  float scale;         // softmax scale (applied to dQ, dK)
+  float scale_log2;    // scale * log2(e)
+  unsigned long long timeout_ns;
+  unsigned int* status;
+  unsigned int* where;
+};
+
+// ---------------------------------------------------------------------------
+// preprocess: one warp per (padded) row
+
+template <int DT, int D>
+__global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const BwdParams p) {
+  using Elem = typename std::conditional<DT == 1, __half, __nv_bfloat16>::type;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<long long>(p.BH) * p.Np) return;
+  const long long bh = row / p.Np;
+  const int i = static_cast<int>(row - bh * p.Np);
+  float2* out = reinterpret_cast<float2*>(p.ws) + row;
+  if (i >= p.N) {
+    if (lane == 0) *out = make_float2(INFINITY, 0.f);
+    return;
+  }
+  const long long g = (bh * p.N + i) * D;
+  const Elem* o = static_cast<const Elem*>(p.o) + g;
+  const Elem* dO = static_cast<const Elem*>(p.dout) + g;
+  float acc = 0.f;
+#pragma unroll
+  for (int c = lane; c < D; c += 32)
+    acc = fmaf(static_cast<float>(o[c]), static_cast<float>(dO[c]), acc);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0)
+    *out = make_float2(p.lse[bh * p.N + i] * 1.4426950408889634f, acc);
+}
+
+// ---------------------------------------------------------------------------
+// shared helpers
+
+struct BwdItem {
+  int bh;
+  int tile;  // query tile (dQ kernel) or key tile (dK/dV kernel)
+  int n;     // number of streamed tiles
+  int first; // first streamed tile
+};
+
+// dQ kernel item: query tile qi streams key tiles 0 .. n-1 (causal: qi+1
+// of them), most work first when causal.
+template <bool CAUSAL>
+__device__ __forceinline__ BwdItem dq_item(int it, const BwdParams& p) {
+  BwdItem w;
+  if (CAUSAL) {
+    w.tile = p.nt - 1 - it / p.BH;
+    w.bh = it % p.BH;
+    w.n = w.tile + 1;
+  } else {
+    w.bh = it / p.nt;
+    w.tile = it % p.nt;
+    w.n = p.nt;
+  }
+  w.first = 0;
+  return w;
+}
+
+// dK/dV kernel item: key tile kj streams query tiles first .. nt-1
+// (causal: from kj on), most work first when causal.
+template <bool CAUSAL>
+__device__ __forceinline__ BwdItem dkv_item(int it, const BwdParams& p) {
+  BwdItem w;
+  if (CAUSAL) {
+    w.tile = it / p.BH;
+    w.bh = it % p.BH;
+    w.first = w.tile;
+  } else {
+    w.bh = it / p.nt;
+    w.tile = it % p.nt;
+    w.first = 0;
+  }
+  w.n = p.nt - w.first;
+  return w;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+template <int DT, int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, int row0, int bh,
+                                          uint32_t bar) {
+  using C = Cfg<DT, D>;
+#pragma unroll
+  for (int b = 0; b < C::kNumBox; ++b)
+    tma_load_3d(dst + b * C::kBoxBytes, map, b * C::kBoxInner, row0, bh, bar);
+}
+
+// A x B^T with both operands K-major in shared memory (S = Q K^T etc.)
+template <int DT, int D>
+__device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t sa, uint32_t sb, uint32_t idesc) {
+  using C = Cfg<DT, D>;
+  const uint64_t a0 = make_sdesc_sw128(sa, 16, 1024);
+  const uint64_t b0 = make_sdesc_sw128(sb, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < C::kNumQKMma; ++k) {
+    const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
+    mma_ss<C::T::kKind>(d_tmem, a0 + off, b0 + off, idesc, k > 0 ? 1u : 0u);
+  }
+}
+
+// D (+)= A B with A (128 x 128, 16-bit) in TMEM and B = a [128 rows x d]
+// tile (d contiguous) as the MN-major B operand
+template <int DT, int D>
+__device__ __forceinline__ void mma_tmn(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
+                                        uint32_t idesc, bool accumulate) {
+  using C = Cfg<DT, D>;
+  const uint64_t b0 = make_sdesc_sw128(sb, C::kBoxBytes, 1024);
+#pragma unroll
+  for (int k = 0; k < C::kNumPVMma; ++k) {
+    const uint32_t off = (k * C::kKPerMma * 128) >> 4;
+    mma_ts<C::T::kKind>(d_tmem, a_tmem + k * 8, b0 + off, idesc, (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
+// 32 fp32 values of a row times `f` -> output type, 64 (16-bit) bytes
+template <int DT>
+__device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&v)[32], float f) {
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]) * f;
+  store_out_chunk<DT>(dst, x);
+}
+
+// ---------------------------------------------------------------------------
+// dQ kernel
+
+template <int NSLOT>
+struct DqCtrl {
+  uint64_t qd_full, qd_empty;
+  uint64_t kv_full[NSLOT], kv_empty[NSLOT];
+  uint64_t s_full;    // S(j), dP(j) in TMEM            (commit)
+  uint64_t sdp_free;  // elementwise read S(j), dP(j)    (4 warps)
+  uint64_t ds_full;   // dS(j) in TMEM                   (4 warps)
+  uint64_t ds_free;   // dQ += dS(j) K_j done            (commit)
+  uint64_t dq_full;   // last dQ MMA of the item done    (commit)
+  uint64_t dq_empty;  // epilogue read dQ                (4 warps)
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+
+template <int DT, int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const BwdParams p) {
+  using C = Cfg<DT, D>;
+  using BC = BwdCfg<DT, D>;
+  constexpr int NS = BC::kSlotsDq;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* sbase = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sQ = smem_u32(sbase), sdO = sQ + C::kTileBytes, sKV = sdO + C::kTileBytes;
+  DqCtrl<NS>* c = reinterpret_cast<DqCtrl<NS>*>(sbase + (2 + NS) * C::kTileBytes);
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&c->qd_full), 1);
+    mbar_init(smem_u32(&c->qd_empty), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&c->kv_full[s]), 1);
+      mbar_init(smem_u32(&c->kv_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&c->s_full), 1);
+    mbar_init(smem_u32(&c->sdp_free), 4);
+    mbar_init(smem_u32(&c->ds_full), 4);
+    mbar_init(smem_u32(&c->ds_free), 1);
+    mbar_init(smem_u32(&c->dq_full), 1);
+    mbar_init(smem_u32(&c->dq_empty), 4);
+    mbar_init(smem_u32(&c->drain), 1);
+    c->abort = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&c->tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = c->tmem_base;
+  const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t qd_uses = 0, loads = 0, round = 0;
+    int slot = 0;
+    bool ok = true;
+    for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
+      const int it = round_item(rnd, p.n_items);
+      if (it < 0) continue;
+      const BwdItem w = dq_item<CAUSAL>(it, p);
+      if (!wait_bar(smem_u32(&c->qd_empty), (qd_uses & 1u) ^ 1u, wc, 0x41)) break;
+      mbar_arrive_expect_tx(smem_u32(&c->qd_full), 2 * C::kTileBytes);
+      load_tile<DT, D>(sQ, &tmQ, w.tile * kBlock, w.bh, smem_u32(&c->qd_full));
+      load_tile<DT, D>(sdO, &tmdO, w.tile * kBlock, w.bh, smem_u32(&c->qd_full));
+      ++qd_uses;
+      for (int j = 0; j < w.n && ok; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          if (!wait_bar(smem_u32(&c->kv_empty[slot]), (round & 1u) ^ 1u, wc, 0x42)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(smem_u32(&c->kv_full[slot]), C::kTileBytes);
+          load_tile<DT, D>(sKV + slot * C::kTileBytes, kv == 0 ? &tmK : &tmV, j * kBlock, w.bh,
+                           smem_u32(&c->kv_full[slot]));
+          ++loads;
+          if (++slot == NS) {
+            slot = 0;
+            ++round;
+          }
+        }
+      }
+    }
+    volatile uint32_t never = 0;
+    const WaitCtx wn{&never, p.timeout_ns, p.status, p.where};
+    for (int s = 0; s < NS; ++s) {
+      const uint32_t uses = loads / NS + (static_cast<uint32_t>(s) < loads % NS ? 1u : 0u);
+      if (uses) wait_bar(smem_u32(&c->kv_full[s]), (uses - 1u) & 1u, wn, 0x43);
+    }
+    if (qd_uses) wait_bar(smem_u32(&c->qd_full), (qd_uses - 1u) & 1u, wn, 0x44);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA
+    uint32_t qd_w = 0, sf_w = 0, ds_w = 0, dqe_w = 0;
+    uint32_t round = 0;
+    int slot = 0;
+    auto next_slot = [&](int& s, uint32_t& par) {
+      s = slot;
+      par = round & 1u;
+      if (++slot == NS) {
+        slot = 0;
+        ++round;
+      }
+    };
+    const uint32_t tS = tbase + BC::kDqS, tDP = tbase + BC::kDqDP, tDS = tbase + BC::kDqDS,
+                   tDQ = tbase + BC::kDqAcc;
+    bool ok = true;
+    for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
+      const int it = round_item(rnd, p.n_items);
+      if (it < 0) continue;
+      const BwdItem w = dq_item<CAUSAL>(it, p);
+      int ks, vs;
+      uint32_t kp, vp;
+      next_slot(ks, kp);
+      next_slot(vs, vp);
+      ok = wait_bar(smem_u32(&c->qd_full), qd_w & 1u, wc, 0x51) &&
+           wait_bar(smem_u32(&c->kv_full[ks]), kp, wc, 0x52) &&
+           wait_bar(smem_u32(&c->kv_full[vs]), vp, wc, 0x52);
+      ++qd_w;
+      if (!ok) break;
+      tc_fence_after_sync();
+      mma_kk<DT, D>(tS, sQ, sKV + ks * C::kTileBytes, BC::kIdescSS);
+      mma_kk<DT, D>(tDP, sdO, sKV + vs * C::kTileBytes, BC::kIdescSS);
+      mma_commit(smem_u32(&c->s_full));
+      mma_commit(smem_u32(&c->kv_empty[vs]));
+      if (w.n == 1) mma_commit(smem_u32(&c->qd_empty));
+      for (int j = 0; j < w.n && ok; ++j) {
+        const int kcur = ks;
+        if (j + 1 < w.n) {
+          // S(j+1), dP(j+1) once the elementwise warps have read S(j), dP(j)
+          next_slot(ks, kp);
+          next_slot(vs, vp);
+          ok = wait_bar(smem_u32(&c->sdp_free), sf_w & 1u, wc, 0x53) &&
+               wait_bar(smem_u32(&c->kv_full[ks]), kp, wc, 0x54) &&
+               wait_bar(smem_u32(&c->kv_full[vs]), vp, wc, 0x54);
+          ++sf_w;
+          if (!ok) break;
+          tc_fence_after_sync();
+          mma_kk<DT, D>(tS, sQ, sKV + ks * C::kTileBytes, BC::kIdescSS);
+          mma_kk<DT, D>(tDP, sdO, sKV + vs * C::kTileBytes, BC::kIdescSS);
+          mma_commit(smem_u32(&c->s_full));
+          mma_commit(smem_u32(&c->kv_empty[vs]));
+          if (j + 2 == w.n) mma_commit(smem_u32(&c->qd_empty));
+        } else {
+          // keep the sdp_free phases in step: the last read of the item
+          ok = wait_bar(smem_u32(&c->sdp_free), sf_w & 1u, wc, 0x53);
+          ++sf_w;
+          if (!ok) break;
+        }
+        // dQ += dS(j) K_j
+        ok = wait_bar(smem_u32(&c->ds_full), ds_w & 1u, wc, 0x55);
+        ++ds_w;
+        if (ok && j == 0) {
+          ok = wait_bar(smem_u32(&c->dq_empty), (dqe_w & 1u) ^ 1u, wc, 0x56);
+          ++dqe_w;
+        }
+        if (!ok) break;
+        tc_fence_after_sync();
+        mma_tmn<DT, D>(tDQ, tDS, sKV + kcur * C::kTileBytes, BC::kIdescTS, j > 0);
+        mma_commit(smem_u32(&c->ds_free));
+        mma_commit(smem_u32(&c->kv_empty[kcur]));
+        if (j + 1 == w.n) mma_commit(smem_u32(&c->dq_full));
+      }
+    }
+    mma_commit(smem_u32(&c->drain));
+    volatile uint32_t never = 0;
+    const WaitCtx wn{&never, p.timeout_ns, p.status, p.where};
+    wait_bar(smem_u32(&c->drain), 0u, wn, 0x57);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ elementwise
+    const uint32_t wq = warp & 3u;
+    const int r = static_cast<int>(wq * 32u + lane);
+    const uint32_t lane_off = (wq * 32u) << 16;
+    const uint32_t tS = tbase + lane_off + BC::kDqS, tDP = tbase + lane_off + BC::kDqDP,
+                   tDS = tbase + lane_off + BC::kDqDS, tDQ = tbase + lane_off + BC::kDqAcc;
+    const float sl2 = p.scale_log2;
+    uint32_t sf_w = 0, dsf_w = 0, dqf_w = 0;
+    bool first_ds = true;
+    for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items; ++rnd) {
+      const int it = round_item(rnd, p.n_items);
+      if (it < 0) continue;
+      const BwdItem w = dq_item<CAUSAL>(it, p);
+      const float2 lv = reinterpret_cast<const float2*>(p.ws)[static_cast<size_t>(w.bh) * p.Np +
+                                                               w.tile * kBlock + r];
+      const float lse2 = lv.x, Dr = lv.y;
+      for (int j = 0; j < w.n; ++j) {
+        if (!wait_bar_all(smem_u32(&c->s_full), sf_w & 1u, wc, 0x61)) goto done;
+        ++sf_w;
+        tc_fence_after_sync();
+        int lim = p.N - j * kBlock;  // keys >= N masked
+        if (CAUSAL && j == w.tile) lim = min(lim, r + 1);
+        uint32_t dsp[64];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sv[64], dpv[64];
+          tmem_ld_x64(tS + 64 * h, sv);
+          tmem_ld_x64(tDP + 64 * h, dpv);
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) {
+            float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), sl2, -lse2));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), sl2, -lse2));
+            if (64 * h + i >= lim) p0 = 0.f;
+            if (64 * h + i + 1 >= lim) p1 = 0.f;
+            const float ds0 = p0 * (__uint_as_float(dpv[i]) - Dr);
+            const float ds1 = p1 * (__uint_as_float(dpv[i + 1]) - Dr);
+            dsp[32 * h + i / 2] = pack2<DT>(ds0, ds1);
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&c->sdp_free));
+        // dS(j-1) must have been consumed before its columns are rewritten
+        if (!first_ds) {
+          if (!wait_bar_all(smem_u32(&c->ds_free), dsf_w & 1u, wc, 0x62)) goto done;
+          ++dsf_w;
+          tc_fence_after_sync();
+        }
+        first_ds = false;
+        {
+          uint32_t lo[32], hi[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            lo[i] = dsp[i];
+            hi[i] = dsp[32 + i];
+          }
+          tmem_st_x32(tDS, lo);
+          tmem_st_x32(tDS + 32, hi);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&c->ds_full));
+      }
+      // epilogue: dQ * scale -> output rows
+      if (!wait_bar_all(smem_u32(&c->dq_full), dqf_w & 1u, wc, 0x63)) goto done;
+      ++dqf_w;
+      tc_fence_after_sync();
+      {
+        const int row = w.tile * kBlock + r;
+        uint8_t* dst = static_cast<uint8_t*>(p.dq) +
+                       (static_cast<size_t>(w.bh) * p.N + row) * D * C::T::kOutEsize;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tDQ + cc, v);
+          if (row < p.N) store_row_chunk<DT>(dst + cc * C::T::kOutEsize, v, p.scale);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c->dq_empty));
+    }
+  }
+done:
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK / dV kernel
+
+template <int NST>
+struct DkvCtrl {
+  uint64_t kv_full, kv_empty;
+  uint64_t st_full[NST], st_empty[NST];  // stage i: Q_i, dO_i, (lse2, D)_i
+  uint64_t s_full;     // S^T(i), dP^T(i) in TMEM          (commit)
+  uint64_t pds_full;   // P^T(i), dS^T(i) in TMEM          (4 warps)
+  uint64_t acc_full;   // last dV / dK MMA of the item done (commit)
+  uint64_t acc_empty;  // epilogue read dV, dK             (4 warps)
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+
+template <int DT, int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                        const BwdParams p) {
+  using C = Cfg<DT, D>;
+  using BC = BwdCfg<DT, D>;
+  constexpr int NST = BC::kStages;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* sbase = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sK = smem_u32(sbase), sV = sK + C::kTileBytes, sSt = sV + C::kTileBytes;
+  uint8_t* st_base = sbase + 2 * C::kTileBytes;
+  DkvCtrl<NST>* c = reinterpret_cast<DkvCtrl<NST>*>(sbase + 2 * C::kTileBytes + NST * BC::kStageBytes);
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&c->kv_full), 1);
+    mbar_init(smem_u32(&c->kv_empty), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(smem_u32(&c->st_full[s]), 1);
+      mbar_init(smem_u32(&c->st_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&c->s_full), 1);
+    mbar_init(smem_u32(&c->pds_full), 4);
+    mbar_init(smem_u32(&c->acc_full), 1);
+    mbar_init(smem_u32(&c->acc_empty), 4);
+    mbar_init(smem_u32(&c->drain), 1);
+    c->abort = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&c->tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = c->tmem_base;
+  const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t kv_uses = 0, loads = 0, round = 0;
+    int st = 0;
+    bool ok = true;
+    for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
+      const int it = round_item(rnd, p.n_items);
+      if (it < 0) continue;
+      const BwdItem w = dkv_item<CAUSAL>(it, p);
+      if (!wait_bar(smem_u32(&c->kv_empty), (kv_uses & 1u) ^ 1u, wc, 0x71)) break;
+      mbar_arrive_expect_tx(smem_u32(&c->kv_full), 2 * C::kTileBytes);
+      load_tile<DT, D>(sK, &tmK, w.tile * kBlock, w.bh, smem_u32(&c->kv_full));
+      load_tile<DT, D>(sV, &tmV, w.tile * kBlock, w.bh, smem_u32(&c->kv_full));
+      ++kv_uses;
+      for (int i = 0; i < w.n; ++i) {
+        const int qi = w.first + i;
+        if (!wait_bar(smem_u32(&c->st_empty[st]), (round & 1u) ^ 1u, wc, 0x72)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bar = smem_u32(&c->st_full[st]);
+        const uint32_t dst = sSt + st * BC::kStageBytes;
+        mbar_arrive_expect_tx(bar, BC::kStageBytes);
+        load_tile<DT, D>(dst, &tmQ, qi * kBlock, w.bh, bar);
+        load_tile<DT, D>(dst + C::kTileBytes, &tmdO, qi * kBlock, w.bh, bar);
+        bulk_load(dst + 2 * C::kTileBytes,
+                  p.ws + (static_cast<size_t>(w.bh) * p.Np + qi * kBlock) * 2, BC::kVecBytes, bar);
+        ++loads;
+        if (++st == NST) {
+          st = 0;
+          ++round;
+        }
+      }
+    }
+    volatile uint32_t never = 0;
+    const WaitCtx wn{&never, p.timeout_ns, p.status, p.where};
+    for (int s = 0; s < NST; ++s) {
+      const uint32_t uses = loads / NST + (static_cast<uint32_t>(s) < loads % NST ? 1u : 0u);
+      if (uses) wait_bar(smem_u32(&c->st_full[s]), (uses - 1u) & 1u, wn, 0x73);
+    }
+    if (kv_uses) wait_bar(smem_u32(&c->kv_full), (kv_uses - 1u) & 1u, wn, 0x74);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA
+    uint32_t kv_w = 0, pds_w = 0, ae_w = 0, round = 0;
+    int st = 0;
+    const uint32_t tS = tbase + BC::kKvS, tDP = tbase + BC::kKvDP, tDV = tbase + BC::kKvDV,
+                   tDK = tbase + BC::kKvDK;
+    bool ok = true;
+    for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
+      const int it = round_item(rnd, p.n_items);
+      if (it < 0) continue;
+      const BwdItem w = dkv_item<CAUSAL>(it, p);
+      ok = wait_bar(smem_u32(&c->kv_full), kv_w & 1u, wc, 0x81) &&
+           wait_bar(smem_u32(&c->st_full[st]), round & 1u, wc, 0x82);
+      ++kv_w;
+      if (!ok) break;
+      tc_fence_after_sync();
+      {
+        const uint32_t sq = sSt + st * BC::kStageBytes;
+        mma_kk<DT, D>(tS, sK, sq, BC::kIdescSS);                      // S^T = K Q_i^T
+        mma_kk<DT, D>(tDP, sV, sq + C::kTileBytes, BC::kIdescSS);     // dP^T = V dO_i^T
+        mma_commit(smem_u32(&c->s_full));
+      }
+      for (int i = 0; i < w.n && ok; ++i) {
+        const uint32_t sq = sSt + st * BC::kStageBytes;
+        ok = wait_bar(smem_u32(&c->pds_full), pds_w & 1u, wc, 0x83);
+        ++pds_w;
+        if (ok && i == 0) {
+          ok = wait_bar(smem_u32(&c->acc_empty), (ae_w & 1u) ^ 1u, wc, 0x84);
+          ++ae_w;
+        }
+        if (!ok) break;
+        tc_fence_after_sync();
+        mma_tmn<DT, D>(tDV, tS, sq + C::kTileBytes, BC::kIdescTS, i > 0);  // dV += P^T dO_i
+        mma_tmn<DT, D>(tDK, tDP, sq, BC::kIdescTS, i > 0);                 // dK += dS^T Q_i
+        mma_commit(smem_u32(&c->st_empty[st]));
+        if (++st == NST) {
+          st = 0;
+          ++round;
+        }
+        if (i + 1 == w.n) {
+          mma_commit(smem_u32(&c->acc_full));
+          mma_commit(smem_u32(&c->kv_empty));
+        } else {
+          // S^T(i+1), dP^T(i+1) go over P^T(i), dS^T(i): issued after the
+          // MMAs that read them, from this same thread
+          ok = wait_bar(smem_u32(&c->st_full[st]), round & 1u, wc, 0x82);
+          if (!ok) break;
+          const uint32_t sn = sSt + st * BC::kStageBytes;
+          mma_kk<DT, D>(tS, sK, sn, BC::kIdescSS);
+          mma_kk<DT, D>(tDP, sV, sn + C::kTileBytes, BC::kIdescSS);
+          mma_commit(smem_u32(&c->s_full));
+        }
+      }
+    }
+    mma_commit(smem_u32(&c->drain));
+    volatile uint32_t never = 0;
+    const WaitCtx wn{&never, p.timeout_ns, p.status, p.where};
+    wait_bar(smem_u32(&c->drain), 0u, wn, 0x85);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ elementwise
+    const uint32_t wq = warp & 3u;
+    const int r = static_cast<int>(wq * 32u + lane);  // key row within the tile
+    const uint32_t lane_off = (wq * 32u) << 16;
+    const uint32_t tS = tbase + lane_off + BC::kKvS, tDP = tbase + lane_off + BC::kKvDP,
+                   tDV = tbase + lane_off + BC::kKvDV, tDK = tbase + lane_off + BC::kKvDK;
+    const float sl2 = p.scale_log2;
+    uint32_t sf_w = 0, af_w = 0, round = 0;
+    int st = 0;
+    for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items; ++rnd) {
+      const int it = round_item(rnd, p.n_items);
+      if (it < 0) continue;
+      const BwdItem w = dkv_item<CAUSAL>(it, p);
+      for (int i = 0; i < w.n; ++i) {
+        const int qi = w.first + i;
+        // S^T(i), dP^T(i) in TMEM, and the stage's (lse2, D) rows landed
+        // (observed here, not only through the MMA thread)
+        if (!wait_bar_all(smem_u32(&c->s_full), sf_w & 1u, wc, 0x91) ||
+            !wait_bar_all(smem_u32(&c->st_full[st]), round & 1u, wc, 0x93))
+          goto done;
+        ++sf_w;
+        tc_fence_after_sync();
+        const float2* vec =
+            reinterpret_cast<const float2*>(st_base + st * BC::kStageBytes + 2 * C::kTileBytes);
+        // causal: query column cq is visible to this key iff cq >= r on the
+        // diagonal tile
+        const int qlim = (CAUSAL && qi == w.tile) ? r : 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sv[64], dpv[64];
+          tmem_ld_x64(tS + 64 * h, sv);
+          tmem_ld_x64(tDP + 64 * h, dpv);
+          uint32_t pp[32], dd[32];
+#pragma unroll
+          for (int i2 = 0; i2 < 64; i2 += 2) {
+            const int cq = 64 * h + i2;
+            const float2 v0 = vec[cq], v1 = vec[cq + 1];
+            float p0 = ex2_approx(fmaf(__uint_as_float(sv[i2]), sl2, -v0.x));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sv[i2 + 1]), sl2, -v1.x));
+            if (cq < qlim) p0 = 0.f;
+            if (cq + 1 < qlim) p1 = 0.f;
+            pp[i2 / 2] = pack2<DT>(p0, p1);
+            dd[i2 / 2] = pack2<DT>(p0 * (__uint_as_float(dpv[i2]) - v0.y),
+                                   p1 * (__uint_as_float(dpv[i2 + 1]) - v1.y));
+          }
+          // P^T half h over S^T columns already read, dS^T over dP^T
+          tmem_st_x32(tS + 32 * h, pp);
+          tmem_st_x32(tDP + 32 * h, dd);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&c->pds_full));
+        if (++st == NST) {
+          st = 0;
+          ++round;
+        }
+      }
+      // epilogue: dV and dK * scale -> output rows
+      if (!wait_bar_all(smem_u32(&c->acc_full), af_w & 1u, wc, 0x92)) goto done;
+      ++af_w;
+      tc_fence_after_sync();
+      {
+        const int row = w.tile * kBlock + r;
+        const size_t off = (static_cast<size_t>(w.bh) * p.N + row) * D * C::T::kOutEsize;
+        uint8_t* dv = static_cast<uint8_t*>(p.dv) + off;
+        uint8_t* dk = static_cast<uint8_t*>(p.dk) + off;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tDV + cc, v);
+          if (row < p.N) store_row_chunk<DT>(dv + cc * C::T::kOutEsize, v, 1.0f);
+          tmem_ld_x32(tDK + cc, v);
+          if (row < p.N) store_row_chunk<DT>(dk + cc * C::T::kOutEsize, v, p.scale);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c->acc_empty));
+    }
+    (void)round;
+  }
+done:
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace wsattn

@@ -48,6 +48,40 @@ enum : int {
 
 constexpr int kMaxDevices = 64;
 
+struct BwdLaunchArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  void* workspace;
+  int B, H, N, d;
+  int causal;
+  int dtype;
+  float scale;
+  cudaStream_t stream;
+  int device;
+  int num_sms;
+  unsigned long long timeout_ns;
+  unsigned int* status;
+  unsigned int* where;
+  EncodeTiledFn encode;
+};
+
+// Workspace of the backward pass: (LSE * log2 e, dO . O) per row, rows
+// padded to whole 128-row tiles per head.
+inline unsigned long long bwd_workspace_bytes(int B, int H, int N) {
+  const unsigned long long np = (static_cast<unsigned long long>(N) + 127ull) / 128ull * 128ull;
+  return static_cast<unsigned long long>(B) * static_cast<unsigned long long>(H) * np * 8ull;
+}
+
+// Backward pass (fp16 / bf16, d = 64 or 128); returns a status code.
+int launch_bwd(const BwdLaunchArgs& a);
+
 // One entry per element type; each returns a status code.
 int launch_fp32(const LaunchArgs& a);
 int launch_fp16(const LaunchArgs& a);
