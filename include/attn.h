@@ -155,6 +155,30 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              unsigned long long workspace_bytes, int B, int H, int N, int d, float scale,
              int causal, int dtype, struct CUstream_st* stream);
 
+/*
+ * attn_bwd_noalloc - attn_bwd for callers that cannot allocate device
+ * memory at call time (a program whose device memory all belongs to its own
+ * pool, a plugin whose host framework owns every allocation, a step that
+ * must not risk an allocation's latency or failure).  It takes no workspace:
+ * the library keeps one 8 MiB array in device global memory for it, created
+ * when the library is loaded on a device and held until the process exits.
+ * The pages describe no counterpart; this is a deployment variant of
+ * attn_bwd, with the same results.
+ *   Limit: B * H * ceil(N / 128) * 128 <= 1,048,576 query rows; larger
+ *   shapes return ATTN_ERR_INVALID_ARG without touching the device.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.  It allocates and frees nothing, here or later.
+ *   All calls on a device share the one array, which keeps whatever the
+ *   last call left in it (nothing in it needs to start zeroed).  Calls whose
+ *   kernels overlap on the device race on it: issue them on one stream or
+ *   order them.
+ * Other arguments, errors and asynchrony as attn_bwd.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                     float scale, int causal, int dtype, struct CUstream_st* stream);
+
 /* attn_status_string - a static, human-readable name for a status code. */
 const char* attn_status_string(int status);
 

@@ -17,7 +17,7 @@ __all__ = [
     "ATTN_FP32", "ATTN_FP16", "ATTN_BF16", "ATTN_FP8_E4M3", "AttnError", "lib_path",
     "load_library", "attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
     "attn_watchdog_selftest", "attn_fwd_raw", "attn_bwd", "attn_bwd_workspace_size",
-    "EXPORTED_SYMBOLS",
+    "attn_bwd_noalloc", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_FP32, ATTN_FP16, ATTN_BF16, ATTN_FP8_E4M3 = 0, 1, 2, 3
@@ -28,7 +28,8 @@ STATUS_NAMES = {
 }
 
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
-                    "attn_watchdog_selftest", "attn_bwd", "attn_bwd_workspace_size")
+                    "attn_watchdog_selftest", "attn_bwd", "attn_bwd_workspace_size",
+                    "attn_bwd_noalloc")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -77,6 +78,9 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i, i, i, i, f, i, i,
                                  vp]
         lib.attn_bwd.restype = i
+        lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i,
+                                         vp]
+        lib.attn_bwd_noalloc.restype = i
         _lib = lib
         return lib
 
@@ -213,4 +217,26 @@ def attn_bwd(q, k, v, o, lse, dout, scale=None, causal: bool = False, dq=None, d
                                  float(scale), int(bool(causal)), code, _stream_handle(stream))
     if st != 0:
         raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dout, scale=None, causal: bool = False, dq=None, dk=None,
+                     dv=None, stream=None):
+    """attn_bwd without a caller workspace: the library's own device array
+    serves as scratch (see include/attn.h for its size limit and for why
+    calls that overlap on the device must be ordered).  Returns (dq, dk, dv)."""
+    import torch
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    st = load_library().attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         dout.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+                                         dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale),
+                                         int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    if st != 0:
+        raise AttnError(st, "attn_bwd_noalloc")
     return dq, dk, dv
