@@ -137,3 +137,59 @@ def attn_bwd(q, k, v, dout, scale: float, causal: bool, n_threads: int = 0):
     if rc != 0:
         raise ValueError("oracle_attn_bwd rejected its arguments")
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# FP8 block quantisation with the 16 x 16 Walsh-Hadamard rotation
+# ("Inside FlashAttention-3 & Warp-Specialized CUDA Kernels", section 5:
+# rotate Q and K by an orthogonal Hadamard transform, Q' = Q H, K' = K H, so
+# that Q' K'^T = Q K^T while outlier channels are spread out, then quantise
+# to e4m3 with a scale per block).  The pages fix neither the block nor the
+# order of the transform's additions; the readings taken (and implemented
+# identically on the GPU, so that codes match bit for bit):
+#   - the transform acts on each group of 16 consecutive channels of a row,
+#     as the fast butterfly: for h = 1, 2, 4, 8, every pair (i, i+h) with
+#     i & h == 0 becomes (a + b, a - b) in fp32; then every value is
+#     multiplied by 1/4 (exact), which makes H orthonormal and symmetric;
+#   - a block is one 128-row tile of one (b, h) (the attention tile);
+#     scale = amax / 448 in fp32 (1 when the block is all zero), code =
+#     e4m3(value / scale), round to nearest even.
+
+def wht16_fp32(x):
+    """The 16-point Walsh-Hadamard butterfly on the last axis groups of 16
+    (last axis length a multiple of 16), fp32, in the order stated above."""
+    v = np.array(x, dtype=np.float32, copy=True)
+    shape = v.shape
+    v = v.reshape(-1, 16)
+    for h in (1, 2, 4, 8):
+        for i in range(16):
+            if i & h == 0:
+                a = v[:, i].copy()
+                b = v[:, i + h].copy()
+                v[:, i] = a + b
+                v[:, i + h] = a - b
+    v = v * np.float32(0.25)
+    return v.reshape(shape)
+
+
+def quantize_fp8_blocks(x, hadamard: bool, block: int = 128):
+    """e4m3 codes and per-block scales of a [B, H, N, d] tensor (values as
+    the GPU reads them, i.e. already rounded to the input type).  Returns
+    (codes: torch.float8_e4m3fn [B, H, N, d], scales: float32 [B, H,
+    ceil(N / block)])."""
+    import torch
+    x = np.asarray(x, dtype=np.float32)
+    B, H, N, d = x.shape
+    v = wht16_fp32(x) if hadamard else x.copy()
+    nt = (N + block - 1) // block
+    scales = np.empty((B, H, nt), dtype=np.float32)
+    q = np.empty_like(v)
+    for t in range(nt):
+        blk = v[:, :, t * block:(t + 1) * block, :]
+        amax = np.abs(blk).max(axis=(2, 3)).astype(np.float32)
+        sc = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+        scales[:, :, t] = sc
+        q[:, :, t * block:(t + 1) * block, :] = blk / sc[:, :, None, None]
+    q = np.clip(q, -448.0, 448.0).astype(np.float32)
+    codes = torch.from_numpy(q).to(torch.float8_e4m3fn)
+    return codes, scales
