@@ -106,6 +106,39 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
                  struct CUstream_st* stream);
 
 /*
+ * attn_fwd_fp8_blockscaled - forward pass on e4m3 Q and K that carry one
+ * fp32 scale per 128-row tile of each (b, h) (the real value of a row in
+ * tile t is code * scale[bh][t]), as attn_quantize_fp8 produces them, and
+ * e4m3 V with one per-tensor descale.  Per key block the softmax uses
+ * scale * q_scale[tile] * k_scale[block]; everything else is attn_fwd_fp8.
+ * Source: tekromancy page, section 5 (block quantisation of FP8 attention
+ * inputs).  q_scales and k_scales: device arrays [B * H, ceil(N / 128)],
+ * 4-byte aligned, finite and > 0.  Other arguments as attn_fwd_fp8.
+ */
+int attn_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int N, int d, float scale, int causal,
+                             const float* q_scales, const float* k_scales, float v_descale,
+                             struct CUstream_st* stream);
+
+/*
+ * attn_quantize_fp8 - e4m3 block quantisation of a [B, H, N, d] tensor (Q
+ * or K), optionally after the 16 x 16 Walsh-Hadamard rotation of each group
+ * of 16 consecutive channels.  The rotation H is orthonormal and symmetric,
+ * so rotating both Q and K keeps Q K^T while spreading outlier channels
+ * (tekromancy page, section 5).  Per 128-row tile of each (b, h): scale =
+ * max|value| / 448 (1 for an all-zero tile), code = e4m3(value / scale)
+ * rounded to nearest even.  The butterfly runs h = 1, 2, 4, 8 over pairs
+ * (i, i + h) as (a + b, a - b) in fp32, then multiplies by 1/4.
+ *   x      : input, dtype ATTN_FP32 / ATTN_FP16 / ATTN_BF16, 16-byte aligned.
+ *   codes  : [B, H, N, d] e4m3 output, 16-byte aligned.
+ *   scales : [B * H, ceil(N / 128)] fp32 output, 4-byte aligned.
+ *   d      : 64 or 128.  hadamard: 0 or 1.
+ * One kernel on `stream`; errors as attn_fwd.
+ */
+int attn_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, int N, int d,
+                      int dtype, int hadamard, struct CUstream_st* stream);
+
+/*
  * attn_fwd_status - synchronises `stream`, then reports and clears the
  * device watchdog word of the current device.  Every wait inside the
  * kernels is bounded (about two seconds); a wait that runs out records

@@ -111,3 +111,25 @@ def _bwd(lib, q=A, k=A, v=A, o=A, do=A, lse=A, dq=A, dk=A, dv=A, ws=A, wsb=1 << 
 ])
 def test_bwd_bad_arguments_are_rejected(lib, kw, code):
     assert _bwd(lib, **kw) == code
+
+
+def _quant(lib, x=A, codes=A, scales=A, B=1, H=1, N=128, d=128, dtype=ws.ATTN_BF16, hadamard=1):
+    return lib.attn_quantize_fp8(x, codes, scales, B, H, N, d, dtype, hadamard, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"x": 0}, 1), ({"codes": 0}, 1), ({"scales": 0}, 1), ({"B": 0}, 1), ({"N": -3}, 1),
+    ({"hadamard": 2}, 1), ({"dtype": 9}, 1), ({"dtype": ws.ATTN_FP8_E4M3}, 2), ({"d": 256}, 2),
+    ({"d": 96}, 2), ({"x": A + 8}, 3), ({"codes": A + 4}, 3), ({"scales": A + 2}, 3),
+])
+def test_quantize_bad_arguments_are_rejected(lib, kw, code):
+    assert _quant(lib, **kw) == code
+
+
+def test_blockscaled_fwd_checks_its_scales(lib):
+    f = lib.attn_fwd_fp8_blockscaled
+    assert f(A, A, A, A, A, 1, 1, 128, 128, 0.1, 0, 0, A, 1.0, None) == 1
+    assert f(A, A, A, A, A, 1, 1, 128, 128, 0.1, 0, A, 0, 1.0, None) == 1
+    assert f(A, A, A, A, A, 1, 1, 128, 128, 0.1, 0, A + 2, A, 1.0, None) == 3
+    assert f(A, A, A, A, A, 1, 1, 128, 128, 0.1, 0, A, A, 0.0, None) == 1
+    assert f(A, A, A, A, A, 1, 1, 128, 64, 0.1, 0, A, A, 1.0, None) == 2

@@ -17,7 +17,7 @@ __all__ = [
     "ATTN_FP32", "ATTN_FP16", "ATTN_BF16", "ATTN_FP8_E4M3", "AttnError", "lib_path",
     "load_library", "attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
     "attn_watchdog_selftest", "attn_fwd_raw", "attn_bwd", "attn_bwd_workspace_size",
-    "attn_bwd_noalloc", "EXPORTED_SYMBOLS",
+    "attn_bwd_noalloc", "attn_fwd_fp8_blockscaled", "attn_quantize_fp8", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_FP32, ATTN_FP16, ATTN_BF16, ATTN_FP8_E4M3 = 0, 1, 2, 3
@@ -29,7 +29,7 @@ STATUS_NAMES = {
 
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
                     "attn_watchdog_selftest", "attn_bwd", "attn_bwd_workspace_size",
-                    "attn_bwd_noalloc")
+                    "attn_bwd_noalloc", "attn_fwd_fp8_blockscaled", "attn_quantize_fp8")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -81,6 +81,11 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i,
                                          vp]
         lib.attn_bwd_noalloc.restype = i
+        lib.attn_fwd_fp8_blockscaled.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, f,
+                                                 vp]
+        lib.attn_fwd_fp8_blockscaled.restype = i
+        lib.attn_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.attn_quantize_fp8.restype = i
         _lib = lib
         return lib
 
@@ -240,3 +245,46 @@ def attn_bwd_noalloc(q, k, v, o, lse, dout, scale=None, causal: bool = False, dq
     if st != 0:
         raise AttnError(st, "attn_bwd_noalloc")
     return dq, dk, dv
+
+
+def attn_quantize_fp8(x, hadamard: bool = True, codes=None, scales=None, stream=None):
+    """e4m3 codes and per-128-row-block scales of a [B, H, N, d] CUDA tensor
+    (optionally after the 16 x 16 Walsh-Hadamard rotation of each group of
+    16 channels).  Returns (codes: float8_e4m3fn, scales: fp32 [B, H, nt])."""
+    import torch
+    if x.dim() != 4 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [B, H, N, d] CUDA tensor")
+    B, H, N, d = x.shape
+    nt = (N + 127) // 128
+    codes = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=x.device) if codes is None else codes
+    scales = torch.empty((B, H, nt), dtype=torch.float32, device=x.device) if scales is None else scales
+    st = load_library().attn_quantize_fp8(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), B, H,
+                                          N, d, _dtype_code(x), int(bool(hadamard)),
+                                          _stream_handle(stream))
+    if st != 0:
+        raise AttnError(st, "attn_quantize_fp8")
+    return codes, scales
+
+
+def attn_fwd_fp8_blockscaled(q, k, v, q_scales, k_scales, v_descale: float, scale=None,
+                             causal: bool = False, out=None, lse=None, stream=None):
+    """Forward pass on e4m3 Q, K with per-128-row-block scales ([B, H, nt]
+    fp32 CUDA tensors, as attn_quantize_fp8 returns them) and e4m3 V with a
+    per-tensor descale.  O is bf16."""
+    import torch
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st = load_library().attn_fwd_fp8_blockscaled(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                 out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                                                 float(scale), int(bool(causal)),
+                                                 q_scales.data_ptr(), k_scales.data_ptr(),
+                                                 float(v_descale), _stream_handle(stream))
+    if st != 0:
+        raise AttnError(st, "attn_fwd_fp8_blockscaled")
+    return out, lse

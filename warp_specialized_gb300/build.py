@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libattn_sm103.so")
 
 SOURCES = ["attn_api.cu", "inst_bf16.cu", "inst_fp16.cu", "inst_fp32.cu", "inst_fp8.cu",
-           "attn_bwd.cu", "attn_bwd_noalloc.cu"]
+           "attn_bwd.cu", "attn_bwd_noalloc.cu", "attn_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -114,7 +114,8 @@ int check_args(const void* q, const void* k, const void* v, const void* o, const
 
 int run(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
         int d, float scale, int causal, int dtype, float q_descale, float k_descale,
-        float v_descale, cudaStream_t stream) {
+        float v_descale, cudaStream_t stream, const float* q_block_scale = nullptr,
+        const float* k_block_scale = nullptr) {
   int rc = check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype);
   if (rc != kOk) return rc;
   if (!finite_positive(q_descale) || !finite_positive(k_descale) || !finite_positive(v_descale))
@@ -139,6 +140,8 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   a.causal = causal;
   a.scale_log2 = static_cast<float>(sl2);
   a.out_scale = v_descale;
+  a.q_block_scale = q_block_scale;
+  a.k_block_scale = k_block_scale;
   a.stream = stream;
   a.device = dev;
   a.num_sms = g_dev[dev].num_sms;
@@ -260,6 +263,17 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              int causal, int dtype, struct CUstream_st* stream) {
   return wsattn::run_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N,
                          d, scale, causal, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int N, int d, float scale, int causal,
+                             const float* q_scales, const float* k_scales, float v_descale,
+                             struct CUstream_st* stream) {
+  if (!q_scales || !k_scales) return wsattn::kErrInvalidArg;
+  if (reinterpret_cast<uintptr_t>(q_scales) % 4 || reinterpret_cast<uintptr_t>(k_scales) % 4)
+    return wsattn::kErrMisaligned;
+  return wsattn::run(q, k, v, o, lse, B, H, N, d, scale, causal, ATTN_FP8_E4M3, 1.0f, 1.0f,
+                     v_descale, reinterpret_cast<cudaStream_t>(stream), q_scales, k_scales);
 }
 
 int attn_fwd_status(struct CUstream_st* stream) {

@@ -131,6 +131,10 @@ struct AttnParams {
   int nkv;        // key blocks per head
   float scale_log2;   // scale * (q, k descales) * log2(e)
   float out_scale;    // v descale (1 for non-fp8)
+  // e4m3 with block scales: one fp32 scale per 128-row tile of Q and of K,
+  // [B*H, n_qt] (null for per-tensor descales)
+  const float* q_block_scale;
+  const float* k_block_scale;
   unsigned long long timeout_ns;
   // library-owned device words: the first error seen by any kernel, and a
   // code saying which wait ran out (role * 16 + barrier kind)
@@ -559,6 +563,13 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
     const int n = w.n[t];
     float m_run = -INFINITY;  // subtraction reference (log2 units)
     float l_run = 0.f;
+    float q_bs = 1.0f;  // block scale of this query tile (e4m3 block scaling)
+    if constexpr (DT == 3) {
+      // the second tile of the last pair lies past N when n_qt is odd: its
+      // rows are never stored, and its scale is not read
+      if (p.q_block_scale && qt < p.n_qt)
+        q_bs = p.q_block_scale[static_cast<size_t>(w.bh) * p.n_qt + qt];
+    }
     float* const inv_l_dst = &c->inv_l[iter & 1u][t][r];
     float* const alpha_dst = &c->alpha[t][r];
     for (int j = 0; j < n; ++j) {
@@ -583,7 +594,14 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
 #pragma unroll
         for (int i = 0; i < kBlock; ++i) s[i] = i < lim ? s[i] : -INFINITY;
       }
-      const float mx = max128(s) * sl2;
+      // scale of this block's scores in base-2 units: with block scales,
+      // the real score is q_scale * k_scale * (code product)
+      float sl2j = sl2;
+      if constexpr (DT == 3) {
+        if (p.k_block_scale)
+          sl2j = sl2 * q_bs * p.k_block_scale[static_cast<size_t>(w.bh) * p.nkv + j];
+      }
+      const float mx = max128(s) * sl2j;
 
       float alpha = 1.0f;
       if (mx > m_run + kRescaleLog2) {
@@ -598,8 +616,8 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
 
       // P over the first kPCols columns of S (already in registers)
       const float neg_m = -m_use;
-      const float sum = exp_store_half<DT, 0>(s, sl2, neg_m, taddr) +
-                        exp_store_half<DT, 64>(s, sl2, neg_m, taddr + C::kPCols / 2);
+      const float sum = exp_store_half<DT, 0>(s, sl2j, neg_m, taddr) +
+                        exp_store_half<DT, 64>(s, sl2j, neg_m, taddr + C::kPCols / 2);
       l_run = alpha * l_run + sum;
       tmem_st_wait();
       // hand 1/l to the epilogue before the last P is announced

@@ -80,6 +80,8 @@ int launch_instance(const LaunchArgs& a) {
   p.n_items = p.BH * p.n_pairs;
   p.scale_log2 = a.scale_log2;
   p.out_scale = a.out_scale;
+  p.q_block_scale = a.q_block_scale;
+  p.k_block_scale = a.k_block_scale;
   p.timeout_ns = a.timeout_ns;
   p.status = a.status;
   p.where = a.where;

@@ -26,6 +26,8 @@ struct LaunchArgs {
   int causal;
   float scale_log2;   // softmax scale (with q/k descales) times log2(e)
   float out_scale;    // v descale
+  const float* q_block_scale;  // e4m3 block scales (null: per-tensor)
+  const float* k_block_scale;
   cudaStream_t stream;
   int device;
   int num_sms;
