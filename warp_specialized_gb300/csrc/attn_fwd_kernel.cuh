@@ -29,6 +29,9 @@
 //                 products of the other: the two-consumer pingpong of the
 //                 card's "Pingpong scheduling" variant, with the turn-taking
 //                 done by the MMA issue order instead of named barriers.
+//                 Each softmax hands its P over in two halves of 64 keys,
+//                 and the MMA thread issues P V_j for the first half while
+//                 the second half's exponentials are computed.
 //   warps 12-15   correction and epilogue: rescales O in Tensor Memory by
 //                 exp2(m_old - m_new) when a row max grew, and at the end
 //                 writes O / l and lets the softmax warps write LSE.
@@ -190,7 +193,7 @@ struct Ctrl {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[NSLOT], kv_empty[NSLOT];
   uint64_t s_full[2];    // S_t(j) in TMEM            (MMA commit)
-  uint64_t p_full[2];    // P_t(j) in TMEM            (4 softmax warps)
+  uint64_t p_full[2][2]; // P_t(j), keys 0-63 / 64-127, in TMEM (4 softmax warps)
   uint64_t sc_full[2];   // alpha_t(j) in smem        (4 softmax warps)
   uint64_t o_full[2];    // PV_t(j) done              (MMA commit)
   uint64_t o_ready[2];   // O_t rescaled for block j  (4 correction warps)
@@ -318,12 +321,16 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t 
   }
 }
 
-template <int DT, int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t sv,
-                                         bool accumulate) {
+// O_t += P_t V_j over one half of the block's keys (HALF 0: keys 0-63, whose
+// P the softmax hands over first; HALF 1: keys 64-127).
+template <int DT, int D, int HALF>
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t sv,
+                                              bool accumulate) {
   using C = Cfg<DT, D>;
+  constexpr int kHalf = C::kNumPVMma / 2;
+  static_assert(C::kNumPVMma % 2 == 0, "PV splits into two key halves");
 #pragma unroll
-  for (int k = 0; k < C::kNumPVMma; ++k) {
+  for (int k = HALF * kHalf; k < (HALF + 1) * kHalf; ++k) {
     // V is [keys, d] with d contiguous: an MN-major B operand.  Each 8-key
     // group is one 1024-byte swizzle atom (SBO); 128-byte column blocks of d
     // are one TMA box apart (LBO).
@@ -389,16 +396,24 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
       if (have_next) next_slot(ns, npar);
       for (int t = 0; t < NQT && ok; ++t) {
         if (j < w.n[t]) {
-          if (!wait_bar(smem_u32(&c->p_full[t]), p_waits[t] & 1u, wc, 0x14) ||
+          // first key half as soon as its P (and the rescaled O) is
+          // there, overlapping the softmax of the second half
+          if (!wait_bar(smem_u32(&c->p_full[t][0]), p_waits[t] & 1u, wc, 0x14) ||
               !wait_bar(smem_u32(&c->o_ready[t]), r_waits[t] & 1u, wc, 0x15)) {
             ok = false;
             break;
           }
-          ++p_waits[t];
           ++r_waits[t];
           tc_fence_after_sync();
-          issue_pv<DT, D>(tbase + C::o_col(t), tbase + C::s_col(t), skv + vs * C::kTileBytes,
-                          j > 0);
+          const uint32_t sv = skv + vs * C::kTileBytes;
+          issue_pv_half<DT, D, 0>(tbase + C::o_col(t), tbase + C::s_col(t), sv, j > 0);
+          if (!wait_bar(smem_u32(&c->p_full[t][1]), p_waits[t] & 1u, wc, 0x18)) {
+            ok = false;
+            break;
+          }
+          ++p_waits[t];
+          tc_fence_after_sync();
+          issue_pv_half<DT, D, 1>(tbase + C::o_col(t), tbase + C::s_col(t), sv, true);
           mma_commit(smem_u32(&c->o_full[t]));
         }
         if (j + 1 < w.n[t]) {
@@ -494,20 +509,25 @@ __device__ __forceinline__ float max128(const float (&s)[128]) {
   return fmaxf(max3f(m[0], m[1], m[2]), m[3]);
 }
 
-// Exponentials of scores OFF .. OFF+63 of one row, written as P into Tensor
-// Memory at taddr_p (16-bit types pack two per column, e4m3 four).
+// Registers per thread of each warpgroup after setmaxnreg (multiples of 8).
+constexpr int kRegsControl = 88;      // producer and MMA-issuer warpgroup
+constexpr int kRegsSoftmax = 168;     // each softmax warpgroup: a 128-score row
+constexpr int kRegsCorrection = 80;   // correction / epilogue warpgroup
+
+// Exponentials of scores OFF .. OFF+LEN-1 of one row, written as P into
+// Tensor Memory at taddr_p (16-bit types pack two per column, e4m3 four).
 // x = s * scale_log2 - m in packed pairs, p = 2^x on MUFU.  Returns the sum
 // of the fp32 exponentials (before rounding to the P type).
-template <int DT, int OFF>
-__device__ __forceinline__ float exp_store_half(const float (&s)[128], float sl2, float neg_m,
-                                                uint32_t taddr_p) {
+template <int DT, int OFF, int LEN>
+__device__ __forceinline__ float exp_store_chunk(const float (&s)[128], float sl2, float neg_m,
+                                                 uint32_t taddr_p) {
   const uint64_t k2 = f2_pack(sl2, sl2);
   const uint64_t b2 = f2_pack(neg_m, neg_m);
   uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-  constexpr int kWords = DT == 3 ? 16 : 32;
+  constexpr int kWords = DT == 3 ? LEN / 4 : LEN / 2;
   uint32_t pk[kWords];
 #pragma unroll
-  for (int ii = 0; ii < 64; ii += 4) {
+  for (int ii = 0; ii < LEN; ii += 4) {
     const int i = OFF + ii;
     float x0, x1, x2, x3;
     f2_unpack(f2_fma(f2_pack(s[i], s[i + 1]), k2, b2), x0, x1);
@@ -523,10 +543,12 @@ __device__ __forceinline__ float exp_store_half(const float (&s)[128], float sl2
       pk[ii / 2 + 1] = pack2<DT>(e2, e3);
     }
   }
-  if constexpr (DT == 3)
+  if constexpr (kWords == 32)
+    tmem_st_x32(taddr_p, pk);
+  else if constexpr (kWords == 16)
     tmem_st_x16(taddr_p, pk);
   else
-    tmem_st_x32(taddr_p, pk);
+    tmem_st_x8(taddr_p, pk);
   float a0, a1;
   f2_unpack(f2_add(acc0, acc1), a0, a1);
   return a0 + a1;
@@ -614,17 +636,23 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c->sc_full[t]));
 
-      // P over the first kPCols columns of S (already in registers)
+      // P over the first kPCols columns of S (already in registers), in two
+      // halves of 64 keys: the first is handed to the MMA issuer while the
+      // second is computed
       const float neg_m = -m_use;
-      const float sum = exp_store_half<DT, 0>(s, sl2j, neg_m, taddr) +
-                        exp_store_half<DT, 64>(s, sl2j, neg_m, taddr + C::kPCols / 2);
-      l_run = alpha * l_run + sum;
+      const float sum0 = exp_store_chunk<DT, 0, 64>(s, sl2j, neg_m, taddr);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t][0]));
+      const float sum1 = exp_store_chunk<DT, 64, 64>(s, sl2j, neg_m, taddr + C::kPCols / 2);
+      l_run = alpha * l_run + (sum0 + sum1);
       tmem_st_wait();
       // hand 1/l to the epilogue before the last P is announced
       if (j == n - 1) *inv_l_dst = __frcp_rn(l_run);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t]));
+      if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t][1]));
     }
     // LSE (natural log) of the real rows
     const int row = qt * kBlock + r;
@@ -764,7 +792,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&c->q_full[t]), 1);
       mbar_init(smem_u32(&c->q_empty[t]), 1);
       mbar_init(smem_u32(&c->s_full[t]), 1);
-      mbar_init(smem_u32(&c->p_full[t]), 4);
+      mbar_init(smem_u32(&c->p_full[t][0]), 4);
+      mbar_init(smem_u32(&c->p_full[t][1]), 4);
       mbar_init(smem_u32(&c->sc_full[t]), 4);
       mbar_init(smem_u32(&c->o_full[t]), 1);
       mbar_init(smem_u32(&c->o_ready[t]), 4);
@@ -792,21 +821,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = c->tmem_base;
 
   // Role dispatch by warpgroup, with the register file split among them:
-  // 88 (producer / MMA) + 168 + 168 (softmax) + 80 (correction) = 504 of
-  // the 4 * 128 registers per thread the block is launched with (the host
-  // refuses to launch a build with any other count).
+  // producer / MMA + 2 * softmax + correction must stay within the 4 * 128
+  // registers per thread the block is launched with (the host refuses to
+  // launch a build with any other count).
+  static_assert(kRegsControl + 2 * kRegsSoftmax + kRegsCorrection <= 4 * 128, "register split");
   const uint32_t wg = warp >> 2;
   if (wg == 0) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     if (warp == 0 && lane == 0)
       role_producer<DT, D, CAUSAL>(&tmQ, &tmK, &tmV, sbase, c, p);
     else if (warp == 1 && lane == 0)
       role_mma<DT, D, CAUSAL>(sbase, c, tbase, p);
   } else if (wg == 1 || wg == 2) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     if (static_cast<int>(wg) - 1 < C::kNQT) role_softmax<DT, D, CAUSAL>(wg - 1, c, tbase, p);
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCorrection));
     role_correction<DT, D, CAUSAL>(c, tbase, p);
   }
 
