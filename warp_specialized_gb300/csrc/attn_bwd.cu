@@ -41,8 +41,8 @@ int launch_bwd_instance(const BwdLaunchArgs& a) {
   la.d = D;
   la.encode = a.encode;
   CUtensorMap mq, mk, mv, mdo;
-  if (!encode_map<DT, D>(la, a.q, &mq) || !encode_map<DT, D>(la, a.k, &mk) ||
-      !encode_map<DT, D>(la, a.v, &mv) || !encode_map<DT, D>(la, a.dout, &mdo))
+  if (!encode_map<DT, D>(la, a.q, kBlock, &mq) || !encode_map<DT, D>(la, a.k, kBlock, &mk) ||
+      !encode_map<DT, D>(la, a.v, kBlock, &mv) || !encode_map<DT, D>(la, a.dout, kBlock, &mdo))
     return kErrCuda;
 
   BwdParams p;

@@ -19,17 +19,18 @@ inline CUtensorMapDataType tensor_map_type(int dt) {
 }
 
 // 3-D view (d, N, B*H) of a dense [B, H, N, d] tensor; the box is one
-// 128-byte swizzle row wide and 128 rows high.  Rows past N inside a head
-// read as zeros (out-of-bounds fill), so a ragged last tile never sees the
-// next head.
+// 128-byte swizzle row wide and box_rows high (128 for Q tiles, 64 for the
+// K/V halves each CTA of a cluster loads).  Rows past N inside a head read
+// as zeros (out-of-bounds fill), so a ragged last tile never sees the next
+// head.
 template <int DT, int D>
-inline bool encode_map(const LaunchArgs& a, const void* ptr, CUtensorMap* map) {
+inline bool encode_map(const LaunchArgs& a, const void* ptr, int box_rows, CUtensorMap* map) {
   using C = Cfg<DT, D>;
   const cuuint64_t es = static_cast<cuuint64_t>(C::kEsize);
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(a.N),
                         static_cast<cuuint64_t>(a.B) * static_cast<cuuint64_t>(a.H)};
   cuuint64_t strides[2] = {D * es, static_cast<cuuint64_t>(a.N) * D * es};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(C::kBoxInner), static_cast<cuuint32_t>(kBlock), 1u};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(C::kBoxInner), static_cast<cuuint32_t>(box_rows), 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = a.encode(map, tensor_map_type(DT), 3, const_cast<void*>(ptr), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -46,6 +47,7 @@ int launch_instance(const LaunchArgs& a) {
   // the warpgroups' setmaxnreg split (88 + 168 + 168 + 80) draws on that
   // pool and could never be satisfied by a smaller one.
   static std::atomic<int> ready[kMaxDevices];
+  static std::atomic<int> max_clusters[kMaxDevices];
   if (a.device < 0 || a.device >= kMaxDevices) return kErrDevice;
   int st = ready[a.device].load(std::memory_order_acquire);
   if (st == 0) {
@@ -59,14 +61,35 @@ int launch_instance(const LaunchArgs& a) {
       cudaGetLastError();
       return kErrCuda;
     }
-    st = (fa.numRegs == 128 && fa.maxThreadsPerBlock >= kThreads) ? 1 : 2;
+    // clusters that can be resident at once (one CTA per SM)
+    int nc = a.num_sms;
+    if (C::kClusterCTAs > 1) {
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = C::kClusterCTAs;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(C::kClusterCTAs * a.num_sms, 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = C::kSmemBytes;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return kErrCuda;
+      }
+    }
+    max_clusters[a.device].store(nc, std::memory_order_relaxed);
+    st = (fa.numRegs == 128 && fa.maxThreadsPerBlock >= kThreads && nc >= 1) ? 1 : 2;
     ready[a.device].store(st, std::memory_order_release);
   }
   if (st != 1) return kErrUnsupported;
 
   CUtensorMap mq, mk, mv;
-  if (!encode_map<DT, D>(a, a.q, &mq) || !encode_map<DT, D>(a, a.k, &mk) ||
-      !encode_map<DT, D>(a, a.v, &mv))
+  const int kv_rows = C::kMulticastKV ? kHalfBlock : kBlock;
+  if (!encode_map<DT, D>(a, a.q, kBlock, &mq) || !encode_map<DT, D>(a, a.k, kv_rows, &mk) ||
+      !encode_map<DT, D>(a, a.v, kv_rows, &mv))
     return kErrCuda;
 
   AttnParams p;
@@ -77,7 +100,8 @@ int launch_instance(const LaunchArgs& a) {
   p.n_qt = (a.N + kBlock - 1) / kBlock;
   p.nkv = p.n_qt;
   p.n_pairs = (p.n_qt + C::kNQT - 1) / C::kNQT;
-  p.n_items = p.BH * p.n_pairs;
+  p.n_groups = (p.n_pairs + C::kClusterCTAs - 1) / C::kClusterCTAs;
+  p.n_items = p.BH * p.n_groups;
   p.scale_log2 = a.scale_log2;
   p.out_scale = a.out_scale;
   p.q_block_scale = a.q_block_scale;
@@ -85,9 +109,24 @@ int launch_instance(const LaunchArgs& a) {
   p.timeout_ns = a.timeout_ns;
   p.status = a.status;
   p.where = a.where;
-  const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
-  kern<<<grid, kThreads, C::kSmemBytes, a.stream>>>(mq, mk, mv, p);
-  if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+  const int nc = max_clusters[a.device].load(std::memory_order_relaxed);
+  const int clusters = p.n_items < nc ? p.n_items : nc;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = C::kClusterCTAs;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C::kClusterCTAs * clusters, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = a.stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = C::kClusterCTAs > 1 ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) != cudaSuccess) {
+    cudaGetLastError();
+    return kErrCuda;
+  }
   return kOk;
 }
 
