@@ -17,7 +17,8 @@ int prepare_kernel(K kern, int smem_bytes, int device, std::atomic<int>* ready) 
       cudaGetLastError();
       return kErrCuda;
     }
-    st = fa.maxThreadsPerBlock >= kBwdThreads ? 1 : 2;
+    // the warpgroups' setmaxnreg split draws on exactly this many registers
+    st = (fa.maxThreadsPerBlock >= kBwdThreads && fa.numRegs == kBwdLaunchRegs) ? 1 : 2;
     ready[device].store(st, std::memory_order_release);
   }
   return st == 1 ? kOk : kErrUnsupported;

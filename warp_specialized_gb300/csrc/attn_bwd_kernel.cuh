@@ -28,9 +28,12 @@
 //                dP^T = V dO_i^T, P^T and dS^T written over them in TMEM,
 //                dV += P^T dO_i and dK += dS^T Q_i accumulated in TMEM.
 // Neither kernel needs atomics; each output element is written once.
-// Roles per CTA (256 threads): warp 0 lane 0 TMA producer, warp 1 lane 0
-// MMA issuer, warps 4-7 the elementwise warpgroup (one thread per row /
-// TMEM lane) that also writes the outputs.  Every wait is bounded.
+// Roles per CTA (384 threads): warp 0 lane 0 TMA producer, warp 1 lane 0
+// MMA issuer, warps 4-7 and 8-11 two elementwise warpgroups that split the
+// 128 columns of every block (columns 0-63 and 64-127; a thread is one row
+// / TMEM lane of its half) and also write the outputs.  The MMA thread
+// starts the products over the first half of the columns as soon as that
+// half is ready.  Every wait is bounded.
 #pragma once
 
 #include <type_traits>
@@ -39,7 +42,16 @@
 
 namespace wsattn {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;
+// Registers per thread after setmaxnreg: the producer / MMA warpgroup gives
+// up registers so that each elementwise thread can hold its half-row of S
+// and dP (128 values) at once.  80 + 2 * 208 = 496 of the 3 * 168 the block
+// is launched with (the host refuses to launch any other count).
+constexpr int kBwdLaunchRegs = 168;
+constexpr int kBwdRegsControl = 80;
+constexpr int kBwdRegsElem = 208;
+static_assert(kBwdRegsControl + 2 * kBwdRegsElem <= 3 * kBwdLaunchRegs, "register split");
+
 
 // The same bounded wait executed by a whole warp, its result made
 // warp-uniform (false for every lane if any lane gave up), for warps that
@@ -71,6 +83,8 @@ struct BwdCfg {
   // instruction descriptors: K-major x K-major (S, dP, S^T, dP^T) and
   // TMEM A x MN-major B (dQ, dV, dK)
   static constexpr uint32_t kIdescSS = make_idesc(C::T::kFmt, C::T::kFmt, false, kBlock, kBlock);
+  // the same with N = 64: one half of the streamed tile's rows as B
+  static constexpr uint32_t kIdescSSHalf = make_idesc(C::T::kFmt, C::T::kFmt, false, 64, kBlock);
   static constexpr uint32_t kIdescTS = make_idesc(C::T::kFmt, C::T::kFmt, true, D, kBlock);
   // TMEM columns, dQ kernel: S | dP | dS (16-bit, 64 columns) | dQ
   static constexpr uint32_t kDqS = 0, kDqDP = 128, kDqDS = 256, kDqAcc = 320;
@@ -218,6 +232,52 @@ __device__ __forceinline__ void mma_tmn(uint32_t d_tmem, uint32_t a_tmem, uint32
   }
 }
 
+// The same over half of the contraction (HALF 0: rows 0-63 of B and TMEM
+// columns 0-31 of A; HALF 1: rows 64-127, columns 32-63)
+template <int DT, int D, int HALF>
+__device__ __forceinline__ void mma_tmn_half(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
+                                             uint32_t idesc, bool accumulate) {
+  using C = Cfg<DT, D>;
+  constexpr int kHalf = C::kNumPVMma / 2;
+  const uint64_t b0 = make_sdesc_sw128(sb, C::kBoxBytes, 1024);
+#pragma unroll
+  for (int k = HALF * kHalf; k < (HALF + 1) * kHalf; ++k) {
+    const uint32_t off = (k * C::kKPerMma * 128) >> 4;
+    mma_ts<C::T::kKind>(d_tmem, a_tmem + k * 8, b0 + off, idesc, (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
+// A x B^T over half of B's 128 rows (HALF 0: rows 0-63, HALF 1: 64-127;
+// each is 8 whole 128-byte swizzle atoms per box), N = 64, into d_tmem.
+template <int DT, int D, int HALF>
+__device__ __forceinline__ void mma_kk_half(uint32_t d_tmem, uint32_t sa, uint32_t sb,
+                                            uint32_t idesc) {
+  using C = Cfg<DT, D>;
+  const uint64_t a0 = make_sdesc_sw128(sa, 16, 1024);
+  const uint64_t b0 = make_sdesc_sw128(sb + HALF * 64 * 128, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < C::kNumQKMma; ++k) {
+    const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
+    mma_ss<C::T::kKind>(d_tmem, a0 + off, b0 + off, idesc, k > 0 ? 1u : 0u);
+  }
+}
+
+// D (+)= A B over one half of the contraction, with that half of A packed
+// in its own 32 TMEM columns from a_half (B rows 64 HALF .. 64 HALF + 63).
+template <int DT, int D, int HALF>
+__device__ __forceinline__ void mma_tmn_part(uint32_t d_tmem, uint32_t a_half, uint32_t sb,
+                                             uint32_t idesc, bool accumulate) {
+  using C = Cfg<DT, D>;
+  constexpr int kHalf = C::kNumPVMma / 2;
+  const uint64_t b0 = make_sdesc_sw128(sb, C::kBoxBytes, 1024);
+#pragma unroll
+  for (int k = HALF * kHalf; k < (HALF + 1) * kHalf; ++k) {
+    const uint32_t off = (k * C::kKPerMma * 128) >> 4;
+    mma_ts<C::T::kKind>(d_tmem, a_half + (k - HALF * kHalf) * 8, b0 + off, idesc,
+                        (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
 // 32 fp32 values of a row times `f` -> output type, 64 (16-bit) bytes
 template <int DT>
 __device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&v)[32], float f) {
@@ -235,11 +295,11 @@ struct DqCtrl {
   uint64_t qd_full, qd_empty;
   uint64_t kv_full[NSLOT], kv_empty[NSLOT];
   uint64_t s_full;    // S(j), dP(j) in TMEM            (commit)
-  uint64_t sdp_free;  // elementwise read S(j), dP(j)    (4 warps)
-  uint64_t ds_full;   // dS(j) in TMEM                   (4 warps)
+  uint64_t sdp_free;  // elementwise read S(j), dP(j)    (8 warps)
+  uint64_t ds_full[2];  // dS(j), keys 0-63 / 64-127, in TMEM (4 warps each)
   uint64_t ds_free;   // dQ += dS(j) K_j done            (commit)
   uint64_t dq_full;   // last dQ MMA of the item done    (commit)
-  uint64_t dq_empty;  // epilogue read dQ                (4 warps)
+  uint64_t dq_empty;  // epilogue read dQ                (8 warps)
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
@@ -268,11 +328,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&c->kv_empty[s]), 1);
     }
     mbar_init(smem_u32(&c->s_full), 1);
-    mbar_init(smem_u32(&c->sdp_free), 4);
-    mbar_init(smem_u32(&c->ds_full), 4);
+    mbar_init(smem_u32(&c->sdp_free), 8);
+    mbar_init(smem_u32(&c->ds_full[0]), 4);
+    mbar_init(smem_u32(&c->ds_full[1]), 4);
     mbar_init(smem_u32(&c->ds_free), 1);
     mbar_init(smem_u32(&c->dq_full), 1);
-    mbar_init(smem_u32(&c->dq_empty), 4);
+    mbar_init(smem_u32(&c->dq_empty), 8);
     mbar_init(smem_u32(&c->drain), 1);
     c->abort = 0u;
     fence_mbar_init();
@@ -287,6 +348,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tbase = c->tmem_base;
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
 
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBwdRegsControl));
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     uint32_t qd_uses = 0, loads = 0, round = 0;
@@ -383,16 +446,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ++sf_w;
           if (!ok) break;
         }
-        // dQ += dS(j) K_j
-        ok = wait_bar(smem_u32(&c->ds_full), ds_w & 1u, wc, 0x55);
-        ++ds_w;
+        // dQ += dS(j) K_j, keys 0-63 as soon as their dS is there
+        ok = wait_bar(smem_u32(&c->ds_full[0]), ds_w & 1u, wc, 0x55);
         if (ok && j == 0) {
           ok = wait_bar(smem_u32(&c->dq_empty), (dqe_w & 1u) ^ 1u, wc, 0x56);
           ++dqe_w;
         }
         if (!ok) break;
         tc_fence_after_sync();
-        mma_tmn<DT, D>(tDQ, tDS, sKV + kcur * C::kTileBytes, BC::kIdescTS, j > 0);
+        mma_tmn_half<DT, D, 0>(tDQ, tDS, sKV + kcur * C::kTileBytes, BC::kIdescTS, j > 0);
+        ok = wait_bar(smem_u32(&c->ds_full[1]), ds_w & 1u, wc, 0x58);
+        ++ds_w;
+        if (!ok) break;
+        tc_fence_after_sync();
+        mma_tmn_half<DT, D, 1>(tDQ, tDS, sKV + kcur * C::kTileBytes, BC::kIdescTS, true);
         mma_commit(smem_u32(&c->ds_free));
         mma_commit(smem_u32(&c->kv_empty[kcur]));
         if (j + 1 == w.n) mma_commit(smem_u32(&c->dq_full));
@@ -402,13 +469,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile uint32_t never = 0;
     const WaitCtx wn{&never, p.timeout_ns, p.status, p.where};
     wait_bar(smem_u32(&c->drain), 0u, wn, 0x57);
-  } else if (warp >= 4) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBwdRegsElem));
     // ------------------------------------------------------------ elementwise
-    const uint32_t wq = warp & 3u;
+    // warpgroup `half` owns key columns [64 half, 64 half + 64) of S, dP
+    // and dS, and dQ columns [d/2 half, d/2 half + d/2) in the epilogue
+    const uint32_t wq = warp & 3u, half = (warp - 4u) >> 2;
     const int r = static_cast<int>(wq * 32u + lane);
     const uint32_t lane_off = (wq * 32u) << 16;
-    const uint32_t tS = tbase + lane_off + BC::kDqS, tDP = tbase + lane_off + BC::kDqDP,
-                   tDS = tbase + lane_off + BC::kDqDS, tDQ = tbase + lane_off + BC::kDqAcc;
+    const uint32_t tS = tbase + lane_off + BC::kDqS + 64 * half,
+                   tDP = tbase + lane_off + BC::kDqDP + 64 * half,
+                   tDS = tbase + lane_off + BC::kDqDS + 32 * half,
+                   tDQ = tbase + lane_off + BC::kDqAcc + (D / 2) * half;
     const float sl2 = p.scale_log2;
     uint32_t sf_w = 0, dsf_w = 0, dqf_w = 0;
     bool first_ds = true;
@@ -423,23 +496,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!wait_bar_all(smem_u32(&c->s_full), sf_w & 1u, wc, 0x61)) goto done;
         ++sf_w;
         tc_fence_after_sync();
-        int lim = p.N - j * kBlock;  // keys >= N masked
-        if (CAUSAL && j == w.tile) lim = min(lim, r + 1);
-        uint32_t dsp[64];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sv[64], dpv[64];
-          tmem_ld_x64(tS + 64 * h, sv);
-          tmem_ld_x64(tDP + 64 * h, dpv);
+        // keys >= N masked; causal: keys after the query on the diagonal
+        int lim = p.N - j * kBlock - 64 * static_cast<int>(half);
+        if (CAUSAL && j == w.tile) lim = min(lim, r + 1 - 64 * static_cast<int>(half));
+        uint32_t dsp[32];
+        {
+          uint32_t v[128];  // S (this half's 64 keys), then dP
+          tmem_ld_2x64_at(tS, tDP, v);
 #pragma unroll
           for (int i = 0; i < 64; i += 2) {
-            float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), sl2, -lse2));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), sl2, -lse2));
-            if (64 * h + i >= lim) p0 = 0.f;
-            if (64 * h + i + 1 >= lim) p1 = 0.f;
-            const float ds0 = p0 * (__uint_as_float(dpv[i]) - Dr);
-            const float ds1 = p1 * (__uint_as_float(dpv[i + 1]) - Dr);
-            dsp[32 * h + i / 2] = pack2<DT>(ds0, ds1);
+            float p0 = ex2_approx(fmaf(__uint_as_float(v[i]), sl2, -lse2));
+            float p1 = ex2_approx(fmaf(__uint_as_float(v[i + 1]), sl2, -lse2));
+            if (i >= lim) p0 = 0.f;
+            if (i + 1 >= lim) p1 = 0.f;
+            const float ds0 = p0 * (__uint_as_float(v[64 + i]) - Dr);
+            const float ds1 = p1 * (__uint_as_float(v[64 + i + 1]) - Dr);
+            dsp[i / 2] = pack2<DT>(ds0, ds1);
           }
         }
         tc_fence_before_sync();
@@ -452,31 +524,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after_sync();
         }
         first_ds = false;
-        {
-          uint32_t lo[32], hi[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            lo[i] = dsp[i];
-            hi[i] = dsp[32 + i];
-          }
-          tmem_st_x32(tDS, lo);
-          tmem_st_x32(tDS + 32, hi);
-        }
+        tmem_st_x32(tDS, dsp);
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&c->ds_full));
+        if (lane == 0) mbar_arrive(smem_u32(&c->ds_full[half]));
       }
-      // epilogue: dQ * scale -> output rows
+      // epilogue: dQ * scale -> output rows (this half's columns)
       if (!wait_bar_all(smem_u32(&c->dq_full), dqf_w & 1u, wc, 0x63)) goto done;
       ++dqf_w;
       tc_fence_after_sync();
       {
         const int row = w.tile * kBlock + r;
         uint8_t* dst = static_cast<uint8_t*>(p.dq) +
-                       (static_cast<size_t>(w.bh) * p.N + row) * D * C::T::kOutEsize;
+                       ((static_cast<size_t>(w.bh) * p.N + row) * D + (D / 2) * half) *
+                           C::T::kOutEsize;
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
+        for (int cc = 0; cc < D / 2; cc += 32) {
           uint32_t v[32];
           tmem_ld_x32(tDQ + cc, v);
           if (row < p.N) store_row_chunk<DT>(dst + cc * C::T::kOutEsize, v, p.scale);
@@ -504,10 +568,10 @@ template <int NST>
 struct DkvCtrl {
   uint64_t kv_full, kv_empty;
   uint64_t st_full[NST], st_empty[NST];  // stage i: Q_i, dO_i, (lse2, D)_i
-  uint64_t s_full;     // S^T(i), dP^T(i) in TMEM          (commit)
-  uint64_t pds_full;   // P^T(i), dS^T(i) in TMEM          (4 warps)
+  uint64_t s_full[2];  // S^T(i), dP^T(i), queries 0-63 / 64-127, in TMEM (commit)
+  uint64_t pds_full[2];  // P^T(i), dS^T(i), queries 0-63 / 64-127, in TMEM (4 warps each)
   uint64_t acc_full;   // last dV / dK MMA of the item done (commit)
-  uint64_t acc_empty;  // epilogue read dV, dK             (4 warps)
+  uint64_t acc_empty;  // epilogue read dV, dK             (8 warps)
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
@@ -536,10 +600,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&c->st_full[s]), 1);
       mbar_init(smem_u32(&c->st_empty[s]), 1);
     }
-    mbar_init(smem_u32(&c->s_full), 1);
-    mbar_init(smem_u32(&c->pds_full), 4);
+    mbar_init(smem_u32(&c->s_full[0]), 1);
+    mbar_init(smem_u32(&c->s_full[1]), 1);
+    mbar_init(smem_u32(&c->pds_full[0]), 4);
+    mbar_init(smem_u32(&c->pds_full[1]), 4);
     mbar_init(smem_u32(&c->acc_full), 1);
-    mbar_init(smem_u32(&c->acc_empty), 4);
+    mbar_init(smem_u32(&c->acc_empty), 8);
     mbar_init(smem_u32(&c->drain), 1);
     c->abort = 0u;
     fence_mbar_init();
@@ -554,6 +620,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tbase = c->tmem_base;
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
 
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBwdRegsControl));
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     uint32_t kv_uses = 0, loads = 0, round = 0;
@@ -611,41 +679,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++kv_w;
       if (!ok) break;
       tc_fence_after_sync();
+      // S^T = K Q_i^T and dP^T = V dO_i^T in two halves of the queries
+      // (columns 0-63 and 64-127).  Half h's P^T / dS^T are packed into the
+      // first 32 columns of its own S^T / dP^T columns, so the next block's
+      // half h may be issued right after this block's products of half h:
+      // the two halves alternate on the tensor pipe while the other half's
+      // elementwise warps work.
+      auto issue_sdp = [&](int h, uint32_t sq) {
+        if (h == 0) {
+          mma_kk_half<DT, D, 0>(tS, sK, sq, BC::kIdescSSHalf);
+          mma_kk_half<DT, D, 0>(tDP, sV, sq + C::kTileBytes, BC::kIdescSSHalf);
+        } else {
+          mma_kk_half<DT, D, 1>(tS + 64, sK, sq, BC::kIdescSSHalf);
+          mma_kk_half<DT, D, 1>(tDP + 64, sV, sq + C::kTileBytes, BC::kIdescSSHalf);
+        }
+        mma_commit(smem_u32(&c->s_full[h]));
+      };
       {
         const uint32_t sq = sSt + st * BC::kStageBytes;
-        mma_kk<DT, D>(tS, sK, sq, BC::kIdescSS);                      // S^T = K Q_i^T
-        mma_kk<DT, D>(tDP, sV, sq + C::kTileBytes, BC::kIdescSS);     // dP^T = V dO_i^T
-        mma_commit(smem_u32(&c->s_full));
+        issue_sdp(0, sq);
+        issue_sdp(1, sq);
       }
       for (int i = 0; i < w.n && ok; ++i) {
         const uint32_t sq = sSt + st * BC::kStageBytes;
-        ok = wait_bar(smem_u32(&c->pds_full), pds_w & 1u, wc, 0x83);
-        ++pds_w;
+        const bool have_next = i + 1 < w.n;
+        const int nst = st + 1 == NST ? 0 : st + 1;
+        const uint32_t nround = st + 1 == NST ? round + 1 : round;
+        const uint32_t sn = sSt + nst * BC::kStageBytes;
+        // queries 0-63: dV += P^T dO_i, dK += dS^T Q_i
+        ok = wait_bar(smem_u32(&c->pds_full[0]), pds_w & 1u, wc, 0x83);
         if (ok && i == 0) {
           ok = wait_bar(smem_u32(&c->acc_empty), (ae_w & 1u) ^ 1u, wc, 0x84);
           ++ae_w;
         }
         if (!ok) break;
         tc_fence_after_sync();
-        mma_tmn<DT, D>(tDV, tS, sq + C::kTileBytes, BC::kIdescTS, i > 0);  // dV += P^T dO_i
-        mma_tmn<DT, D>(tDK, tDP, sq, BC::kIdescTS, i > 0);                 // dK += dS^T Q_i
-        mma_commit(smem_u32(&c->st_empty[st]));
-        if (++st == NST) {
-          st = 0;
-          ++round;
+        mma_tmn_part<DT, D, 0>(tDV, tS, sq + C::kTileBytes, BC::kIdescTS, i > 0);
+        mma_tmn_part<DT, D, 0>(tDK, tDP, sq, BC::kIdescTS, i > 0);
+        if (have_next) {
+          if (!wait_bar(smem_u32(&c->st_full[nst]), nround & 1u, wc, 0x82)) break;
+          issue_sdp(0, sn);
         }
-        if (i + 1 == w.n) {
+        // queries 64-127
+        ok = wait_bar(smem_u32(&c->pds_full[1]), pds_w & 1u, wc, 0x86);
+        ++pds_w;
+        if (!ok) break;
+        tc_fence_after_sync();
+        mma_tmn_part<DT, D, 1>(tDV, tS + 64, sq + C::kTileBytes, BC::kIdescTS, true);
+        mma_tmn_part<DT, D, 1>(tDK, tDP + 64, sq, BC::kIdescTS, true);
+        mma_commit(smem_u32(&c->st_empty[st]));
+        st = nst;
+        round = nround;
+        if (have_next) {
+          issue_sdp(1, sn);
+        } else {
           mma_commit(smem_u32(&c->acc_full));
           mma_commit(smem_u32(&c->kv_empty));
-        } else {
-          // S^T(i+1), dP^T(i+1) go over P^T(i), dS^T(i): issued after the
-          // MMAs that read them, from this same thread
-          ok = wait_bar(smem_u32(&c->st_full[st]), round & 1u, wc, 0x82);
-          if (!ok) break;
-          const uint32_t sn = sSt + st * BC::kStageBytes;
-          mma_kk<DT, D>(tS, sK, sn, BC::kIdescSS);
-          mma_kk<DT, D>(tDP, sV, sn + C::kTileBytes, BC::kIdescSS);
-          mma_commit(smem_u32(&c->s_full));
         }
       }
     }
@@ -653,13 +742,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile uint32_t never = 0;
     const WaitCtx wn{&never, p.timeout_ns, p.status, p.where};
     wait_bar(smem_u32(&c->drain), 0u, wn, 0x85);
-  } else if (warp >= 4) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBwdRegsElem));
     // ------------------------------------------------------------ elementwise
-    const uint32_t wq = warp & 3u;
+    // warpgroup `half` owns query columns [64 half, 64 half + 64) of S^T and
+    // dP^T; their P^T and dS^T go, packed, to the first 32 of those columns,
+    // and dV / dK columns [d/2 half, d/2 half + d/2) are its share of the
+    // epilogue.
+    const uint32_t wq = warp & 3u, half = (warp - 4u) >> 2;
     const int r = static_cast<int>(wq * 32u + lane);  // key row within the tile
     const uint32_t lane_off = (wq * 32u) << 16;
     const uint32_t tS = tbase + lane_off + BC::kKvS, tDP = tbase + lane_off + BC::kKvDP,
-                   tDV = tbase + lane_off + BC::kKvDV, tDK = tbase + lane_off + BC::kKvDK;
+                   tDV = tbase + lane_off + BC::kKvDV + (D / 2) * half,
+                   tDK = tbase + lane_off + BC::kKvDK + (D / 2) * half;
     const float sl2 = p.scale_log2;
     uint32_t sf_w = 0, af_w = 0, round = 0;
     int st = 0;
@@ -671,7 +767,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int qi = w.first + i;
         // S^T(i), dP^T(i) in TMEM, and the stage's (lse2, D) rows landed
         // (observed here, not only through the MMA thread)
-        if (!wait_bar_all(smem_u32(&c->s_full), sf_w & 1u, wc, 0x91) ||
+        if (!wait_bar_all(smem_u32(&c->s_full[half]), sf_w & 1u, wc, 0x91) ||
             !wait_bar_all(smem_u32(&c->st_full[st]), round & 1u, wc, 0x93))
           goto done;
         ++sf_w;
@@ -681,48 +777,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // causal: query column cq is visible to this key iff cq >= r on the
         // diagonal tile
         const int qlim = (CAUSAL && qi == w.tile) ? r : 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sv[64], dpv[64];
-          tmem_ld_x64(tS + 64 * h, sv);
-          tmem_ld_x64(tDP + 64 * h, dpv);
-          uint32_t pp[32], dd[32];
+        uint32_t pp[32], dd[32];
+        {
+          uint32_t v[128];  // S^T (this half's 64 queries), then dP^T
+          tmem_ld_2x64_at(tS + 64 * half, tDP + 64 * half, v);
+          const float4* vec4 = reinterpret_cast<const float4*>(vec) + 32 * half;
 #pragma unroll
           for (int i2 = 0; i2 < 64; i2 += 2) {
-            const int cq = 64 * h + i2;
-            const float2 v0 = vec[cq], v1 = vec[cq + 1];
-            float p0 = ex2_approx(fmaf(__uint_as_float(sv[i2]), sl2, -v0.x));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sv[i2 + 1]), sl2, -v1.x));
+            const int cq = 64 * static_cast<int>(half) + i2;
+            const float4 lv = vec4[i2 / 2];  // (lse2, D) of query columns cq, cq + 1
+            float p0 = ex2_approx(fmaf(__uint_as_float(v[i2]), sl2, -lv.x));
+            float p1 = ex2_approx(fmaf(__uint_as_float(v[i2 + 1]), sl2, -lv.z));
             if (cq < qlim) p0 = 0.f;
             if (cq + 1 < qlim) p1 = 0.f;
             pp[i2 / 2] = pack2<DT>(p0, p1);
-            dd[i2 / 2] = pack2<DT>(p0 * (__uint_as_float(dpv[i2]) - v0.y),
-                                   p1 * (__uint_as_float(dpv[i2 + 1]) - v1.y));
+            dd[i2 / 2] = pack2<DT>(p0 * (__uint_as_float(v[64 + i2]) - lv.y),
+                                   p1 * (__uint_as_float(v[64 + i2 + 1]) - lv.w));
           }
-          // P^T half h over S^T columns already read, dS^T over dP^T
-          tmem_st_x32(tS + 32 * h, pp);
-          tmem_st_x32(tDP + 32 * h, dd);
         }
+        // P^T over this half's S^T columns (already read), dS^T over dP^T
+        tmem_st_x32(tS + 64 * half, pp);
+        tmem_st_x32(tDP + 64 * half, dd);
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&c->pds_full));
+        if (lane == 0) mbar_arrive(smem_u32(&c->pds_full[half]));
         if (++st == NST) {
           st = 0;
           ++round;
         }
       }
-      // epilogue: dV and dK * scale -> output rows
+      // epilogue: dV and dK * scale -> output rows (this half's columns)
       if (!wait_bar_all(smem_u32(&c->acc_full), af_w & 1u, wc, 0x92)) goto done;
       ++af_w;
       tc_fence_after_sync();
       {
         const int row = w.tile * kBlock + r;
-        const size_t off = (static_cast<size_t>(w.bh) * p.N + row) * D * C::T::kOutEsize;
+        const size_t off =
+            ((static_cast<size_t>(w.bh) * p.N + row) * D + (D / 2) * half) * C::T::kOutEsize;
         uint8_t* dv = static_cast<uint8_t*>(p.dv) + off;
         uint8_t* dk = static_cast<uint8_t*>(p.dk) + off;
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
+        for (int cc = 0; cc < D / 2; cc += 32) {
           uint32_t v[32];
           tmem_ld_x32(tDV + cc, v);
           if (row < p.N) store_row_chunk<DT>(dv + cc * C::T::kOutEsize, v, 1.0f);
