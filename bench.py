@@ -226,6 +226,17 @@ def run_gpu(args):
         raise RuntimeError("watchdog fired during the timed region")
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_s = sum(kernel_ms) / 1e3
+    # the same steps back to back, without the L2 flush between them
+    # (reported beside the flushed number, not used for `value`)
+    nf_steps = max(3, min(args.steps, 50))
+    nf0, nf1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nf0.record(stream)
+    for _ in range(nf_steps):
+        step()
+    nf1.record(stream)
+    torch.cuda.synchronize()
+    no_flush_ms = nf0.elapsed_time(nf1) / nf_steps
+    sorted_ms = sorted(kernel_ms)
     max_total_s = max_over_ranks(total_s, world, dev)
     value = weak_scaling_value(flops, args.steps, world, max_total_s)
     avg_ms = max_total_s / args.steps * 1e3
@@ -312,11 +323,15 @@ def run_gpu(args):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "schedule": "steps pipelined over two buffer sets: H2D(i+1) || kernel(i) || D2H(i-1)"},
-        "gpu_launches": args.steps + e2e_steps,
+        "gpu_launches": args.steps + nf_steps + e2e_steps,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": UNIT, "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(), "peak_source": peak_src,
                      "kernel": KERNEL_NAME},
+        "timing": {"ms_per_step_median": round(sorted_ms[len(sorted_ms) // 2], 4),
+                   "ms_per_step_min": round(sorted_ms[0], 4),
+                   "ms_per_step_no_l2_flush": round(no_flush_ms, 4),
+                   "no_l2_flush_steps": nf_steps},
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
     }
@@ -417,7 +432,9 @@ def main():
             tf, dt, n_rows, cores, desc = oracle_sample(args.cpu_seconds)
             result["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores,
                                       "kind": "oracle", "sample": desc,
-                                      "seconds": round(dt, 2)}
+                                      "seconds": round(dt, 2),
+                                      "full_workload_s_extrapolated":
+                                          round(result["config"]["flops_per_step"] / (tf * 1e12), 1)}
         print(json.dumps(result), flush=True)
 
 
