@@ -34,6 +34,27 @@ def test_quantisation_is_bit_exact(dtype, d, hadamard):
     np.testing.assert_array_equal(scales.cpu().numpy(), want_scales)
 
 
+@pytest.mark.parametrize("hadamard", [False, True], ids=["plain", "hadamard"])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 128), ("fp32", 64), ("bf16", 64)])
+def test_quantisation_bit_exact_across_block_magnitudes(dtype, d, hadamard):
+    """Many tiles whose magnitudes step by powers of two from block to block
+    (one all-zero block per head), with a ragged last tile."""
+    x = ai.make_inputs(2, 2, 33 * 128 + 77, d, dtype, seed=40 + d, outliers=4).q.float()
+    B, H, N, _ = x.shape
+    nt = (N + 127) // 128
+    lo, hi = (-8, 6) if dtype == "fp16" else (-30, 30)
+    e = torch.tensor([lo + (t * 7) % (hi - lo + 1) for t in range(nt)], dtype=torch.float32)
+    f = torch.pow(2.0, e).repeat_interleave(128)[:N]
+    f[5 * 128:6 * 128] = 0.0
+    x = (x * f[None, None, :, None]).to(ai.DTYPES[dtype])
+    codes, scales = ws.attn_quantize_fp8(x.cuda(), hadamard=hadamard)
+    torch.cuda.synchronize()
+    want_codes, want_scales = oracle.quantize_fp8_blocks(x.float().numpy(), hadamard)
+    assert torch.equal(codes.cpu().view(torch.uint8), want_codes.view(torch.uint8))
+    np.testing.assert_array_equal(scales.cpu().numpy(), want_scales)
+    assert (scales.cpu()[:, :, 5] == 1.0).all()
+
+
 def _dequant(codes, scales):
     B, H, N, d = codes.shape
     c = codes.to(torch.float64)

@@ -4,19 +4,20 @@
 // Q' K'^T = Q K^T while spreading outlier channels over 16 channels, and
 // block scales replace one per-tensor scale).
 //
-// One CTA per (b, h, 128-row tile): each thread holds one row in registers,
-// rotates each group of 16 channels with the fast butterfly (h = 1, 2, 4, 8:
-// (a, b) -> (a + b, a - b) in fp32, then * 1/4), the block's absolute
-// maximum is reduced over the CTA, scale = amax / 448 (IEEE division; 1 for
-// an all-zero block) and code = e4m3(value / scale), round to nearest even,
-// saturating.  HBM-bound: it reads the tensor once and writes one byte per
-// element plus one scale per block.
+// One CTA per (b, h, 128-row tile), reading the tile with coalesced 16-byte
+// loads: each group of 16 channels is rotated with the fast butterfly
+// (h = 1, 2, 4, 8: (a, b) -> (a + b, a - b) in fp32, then * 1/4), the
+// block's absolute maximum is reduced over the CTA, scale = amax / 448 (IEEE
+// division; 1 for an all-zero block) and code = e4m3(value / scale), the
+// quotient correctly rounded in fp32, then to e4m3 nearest even, saturating.  HBM-bound: it reads the tensor once and
+// writes one byte per element plus one scale per block.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "attn.h"
 #include "attn_launch.h"
@@ -24,58 +25,52 @@
 namespace wsattn {
 namespace {
 
-// Group g of 16 channels of a row held as raw 16-byte words, as fp32
+// A 16-byte chunk of a row (8 elements of a 16-bit type, 4 of fp32) as fp32
 template <typename T>
-__device__ __forceinline__ void unpack16(const uint4* raw, int g, float (&v)[16]);
+__device__ __forceinline__ void unpack_chunk(const uint4 x, float (&v)[16 / sizeof(T)]);
 
 template <>
-__device__ __forceinline__ void unpack16<float>(const uint4* raw, int g, float (&v)[16]) {
+__device__ __forceinline__ void unpack_chunk<float>(const uint4 x, float (&v)[4]) {
+  v[0] = __uint_as_float(x.x);
+  v[1] = __uint_as_float(x.y);
+  v[2] = __uint_as_float(x.z);
+  v[3] = __uint_as_float(x.w);
+}
+
+template <>
+__device__ __forceinline__ void unpack_chunk<__nv_bfloat16>(const uint4 x, float (&v)[8]) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 x = raw[4 * g + i];
-    v[4 * i] = __uint_as_float(x.x);
-    v[4 * i + 1] = __uint_as_float(x.y);
-    v[4 * i + 2] = __uint_as_float(x.z);
-    v[4 * i + 3] = __uint_as_float(x.w);
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
   }
 }
 
 template <>
-__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4* raw, int g, float (&v)[16]) {
+__device__ __forceinline__ void unpack_chunk<__half>(const uint4 x, float (&v)[8]) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint4 x = raw[2 * g + i];
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-    }
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+    v[2 * j] = f.x;
+    v[2 * j + 1] = f.y;
   }
 }
 
-template <>
-__device__ __forceinline__ void unpack16<__half>(const uint4* raw, int g, float (&v)[16]) {
+// The 16-point Walsh-Hadamard butterfly on a group of 16 channels spread
+// over 16 / E adjacent lanes, E channels each (v = this lane's E channels,
+// lane bit h / E of the lane index says which part of the group it holds).
+// Stages h = 1, 2, 4, 8 in that order, each (a, b) -> (a + b, a - b) in fp32
+// for the pair (i, i + h): stages below E pair channels inside a lane, the
+// others pair a lane with lane ^ (h / E), where the lane holding i keeps
+// a + b and the lane holding i + h keeps a - b.  Then * 1/4.
+template <int E>
+__device__ __forceinline__ void wht16_lanes(float (&v)[E]) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint4 x = raw[2 * g + i];
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  for (int h = 1; h < E; h <<= 1) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
-      const float2 f = __half22float2(h);
-      v[8 * i + 2 * j] = f.x;
-      v[8 * i + 2 * j + 1] = f.y;
-    }
-  }
-}
-
-// 16-point Walsh-Hadamard butterfly on v[0 .. 15], fp32, then * 1/4
-__device__ __forceinline__ void wht16(float (&v)[16]) {
-#pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < E; ++i) {
       if ((i & h) == 0) {
         const float a = v[i], b = v[i + h];
         v[i] = __fadd_rn(a, b);
@@ -83,84 +78,159 @@ __device__ __forceinline__ void wht16(float (&v)[16]) {
       }
     }
   }
+  const int lane = static_cast<int>(threadIdx.x & 31);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+  for (int h = E; h < 16; h <<= 1) {
+    // other + v or other - v, rounded once: fma with a multiplier of +-1
+    const float sgn = (lane & (h / E)) != 0 ? -1.0f : 1.0f;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const float other = __shfl_xor_sync(0xffffffffu, v[i], h / E);
+      v[i] = __fmaf_rn(sgn, v[i], other);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < E; ++i) v[i] = __fmul_rn(v[i], 0.25f);
 }
 
-// One CTA per (b, h, 128-row tile), one thread per row.  The row stays in
-// registers as the raw words it was loaded as (64 registers for a bf16 row
-// of 128 channels), so that small CTAs keep several tiles of loads in
-// flight on each SM; for 16-bit inputs the rotation of each group of 16
-// channels is computed once for the block maximum and again, identically,
-// for the codes (fp32 rows keep the rotated values in place).
-template <typename T, int D>
-__global__ void __launch_bounds__(128) quant_fp8_kernel(const T* __restrict__ x,
-                                                       uint8_t* __restrict__ codes,
-                                                       float* __restrict__ scales, int N, int nt,
-                                                       int hadamard) {
-  constexpr int kWords = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte words per row
-  __shared__ float red[4];
+// value / scale correctly rounded, from y = 1 / scale correctly rounded, by
+// Markstein's refinement (P. Markstein, "Computation of elementary functions
+// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+// with r = a - q b computed exactly by an fma, RN(q + r y) is the correctly
+// rounded quotient whenever q is within one ulp of a / b.  q = RN(a y) can be
+// off by up to 1.5 ulp, so one refinement first makes it faithful and a
+// second rounds it correctly.  Valid while neither the quotient's ulp times
+// b nor y leaves the normal range: the caller takes this path only for
+// 2^-60 <= scale <= 2^60 with |value| <= 448 scale, where every quotient that
+// can reach a nonzero e4m3 code (|a / b| > 2^-10) has an exact remainder, and
+// smaller ones round to a zero code whatever their last bits; copysign keeps
+// the sign of a zero quotient.
+__device__ __forceinline__ float div_scale(float a, float b, float y) {
+  float q = __fmul_rn(a, y);
+  float r = __fmaf_rn(-q, b, a);
+  q = __fmaf_rn(r, y, q);
+  r = __fmaf_rn(-q, b, a);
+  q = __fmaf_rn(r, y, q);
+  return copysignf(q, a);
+}
+
+// e4m3 codes of one chunk's E values, stored as E bytes
+template <int E, bool REFINE>
+__device__ __forceinline__ void store_codes(const float (&v)[E], float scale, float y,
+                                            uint8_t* dst) {
+  float q[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) q[i] = REFINE ? div_scale(v[i], scale, y) : __fdiv_rn(v[i], scale);
+  uint32_t pk[E / 4];
+#pragma unroll
+  for (int j = 0; j < E / 4; ++j) {
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(q[4 * j], q[4 * j + 1]), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(q[4 * j + 2], q[4 * j + 3]), __NV_SATFINITE, __NV_E4M3);
+    pk[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  if constexpr (E == 8)
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+  else
+    *reinterpret_cast<uint32_t*>(dst) = pk[0];
+}
+
+// One CTA of NT threads per (b, h, 128-row tile).  The tile's rows are one
+// contiguous span of memory, cut into 16-byte chunks; thread t takes chunks
+// t, t + NT, t + 2 NT, ..., so that every warp-wide load and store covers
+// one contiguous run.  NT is a multiple of the W chunks of a row, so a
+// thread always holds the same E channels (chunk t mod W) of its rows, and
+// the 16 / E chunks of a group of 16 channels sit in adjacent lanes.  The
+// tile is read once and kept in registers (raw words, or the rotated fp32
+// values) until the block maximum is known.
+template <typename T, int D, int NT, bool HAD>
+__global__ void __launch_bounds__(NT) quant_fp8_kernel(const T* __restrict__ x,
+                                                      uint8_t* __restrict__ codes,
+                                                      float* __restrict__ scales, int N,
+                                                      int nt) {
+  constexpr int E = 16 / static_cast<int>(sizeof(T));  // channels per chunk
+  constexpr int W = D / E;                              // chunks per row
+  constexpr int C = 128 * W / NT;                       // chunks per thread
+  constexpr int kRowStep = NT / W;                      // rows between a thread's chunks
+  static_assert(NT % W == 0 && (128 * W) % NT == 0 && 16 % E == 0, "chunk layout");
+  __shared__ float red[NT / 32];
   const long long blk = blockIdx.x;
   const long long bh = blk / nt;
   const int tile = static_cast<int>(blk - bh * nt);
-  const int row = tile * 128 + static_cast<int>(threadIdx.x);
-  const bool valid = row < N;
-  const size_t off = (static_cast<size_t>(bh) * N + (valid ? row : 0)) * D;
-  uint4 raw[kWords];
-  const uint4* src = reinterpret_cast<const uint4*>(x + off);
+  const int row0 = tile * 128 + static_cast<int>(threadIdx.x) / W;
+  const size_t base = (static_cast<size_t>(bh) * N + static_cast<size_t>(tile) * 128) * D;
+  const uint4* src = reinterpret_cast<const uint4*>(x + base) + threadIdx.x;
+  uint4 raw[C];
 #pragma unroll
-  for (int i = 0; i < kWords; ++i) raw[i] = valid ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+  for (int k = 0; k < C; ++k)
+    raw[k] = row0 + k * kRowStep < N ? src[k * NT] : make_uint4(0u, 0u, 0u, 0u);
+  float rot[HAD ? C : 1][E];
   float amax = 0.f;
-  constexpr bool kInPlace = sizeof(T) == 4;  // fp32 rows keep the rotated values themselves
 #pragma unroll
-  for (int g = 0; g < D / 16; ++g) {
-    float v[16];
-    unpack16<T>(raw, g, v);
-    if (hadamard) wht16(v);
+  for (int k = 0; k < C; ++k) {
+    float v[E];
+    unpack_chunk<T>(raw[k], v);
+    if constexpr (HAD) wht16_lanes<E>(v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    if constexpr (kInPlace) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        raw[4 * g + i] = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
-                                    __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+    for (int i = 0; i < E; ++i) {
+      amax = fmaxf(amax, fabsf(v[i]));
+      if constexpr (HAD) rot[k][i] = v[i];
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
-  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < NT / 32; ++w) amax = fmaxf(amax, red[w]);
   const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  const bool refine = scale >= 0x1p-60f && scale <= 0x1p60f;  // same for the whole block
+  const float y = __frcp_rn(scale);
   if (threadIdx.x == 0) scales[blk] = scale;
-  if (!valid) return;
+  uint8_t* dst = codes + base + static_cast<size_t>(threadIdx.x) * E;
+  // one branch for the block, so that the per-element code has none
+  auto store_all = [&](auto refine_tag) {
+    constexpr bool kRefine = decltype(refine_tag)::value;
 #pragma unroll
-  for (int g = 0; g < D / 16; ++g) {
-    float v[16];
-    unpack16<T>(raw, g, v);
-    if (hadamard && !kInPlace) wht16(v);
-    uint32_t pk[4];
+    for (int k = 0; k < C; ++k) {
+      if (row0 + k * kRowStep >= N) break;
+      float v[E];
+      if constexpr (HAD) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-          make_float2(__fdiv_rn(v[4 * i], scale), __fdiv_rn(v[4 * i + 1], scale)),
-          __NV_SATFINITE, __NV_E4M3);
-      const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-          make_float2(__fdiv_rn(v[4 * i + 2], scale), __fdiv_rn(v[4 * i + 3], scale)),
-          __NV_SATFINITE, __NV_E4M3);
-      pk[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        for (int i = 0; i < E; ++i) v[i] = rot[k][i];
+      } else {
+        unpack_chunk<T>(raw[k], v);
+      }
+      store_codes<E, kRefine>(v, scale, y, dst + static_cast<size_t>(k) * NT * E);
     }
-    *reinterpret_cast<uint4*>(codes + off + 16 * g) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  }
+  };
+  if (refine)
+    store_all(std::true_type{});
+  else
+    store_all(std::false_type{});
 }
 
 template <typename T, int D>
 int launch_quant(const void* x, void* codes, float* scales, int B, int H, int N, int hadamard,
                  cudaStream_t stream) {
+  // Four 16-byte chunks per thread for 16-bit rows and eight for fp32 rows
+  // (capped at 512 threads) measured fastest: bf16 d = 128 takes 512
+  // threads, d = 64 takes 256.
+  constexpr int kW = D * static_cast<int>(sizeof(T)) / 16;
+  constexpr int kPerThread = sizeof(T) == 4 ? 8 : 4;
+  constexpr int kNT = 128 * kW / kPerThread > 512 ? 512 : 128 * kW / kPerThread;
   const int nt = (N + 127) / 128;
   const long long blocks = static_cast<long long>(B) * H * nt;
-  quant_fp8_kernel<T, D><<<static_cast<unsigned>(blocks), 128, 0, stream>>>(
-      static_cast<const T*>(x), static_cast<uint8_t*>(codes), scales, N, nt, hadamard);
+  const auto* xp = static_cast<const T*>(x);
+  auto* cp = static_cast<uint8_t*>(codes);
+  if (hadamard)
+    quant_fp8_kernel<T, D, kNT, true><<<static_cast<unsigned>(blocks), kNT, 0, stream>>>(
+        xp, cp, scales, N, nt);
+  else
+    quant_fp8_kernel<T, D, kNT, false><<<static_cast<unsigned>(blocks), kNT, 0, stream>>>(
+        xp, cp, scales, N, nt);
   return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
