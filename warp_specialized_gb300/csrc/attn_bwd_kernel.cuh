@@ -290,10 +290,14 @@ __device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&v)[3
 // ---------------------------------------------------------------------------
 // dQ kernel
 
-template <int NSLOT>
+// K and V stream through rings of their own: V_j is free as soon as dP(j)
+// is done, K_j only after dQ += dS(j) K_j, and one shared ring would hold
+// each V load back behind a K slot.
+template <int NK, int NV>
 struct DqCtrl {
   uint64_t qd_full, qd_empty;
-  uint64_t kv_full[NSLOT], kv_empty[NSLOT];
+  uint64_t k_full[NK], k_empty[NK];
+  uint64_t v_full[NV], v_empty[NV];
   uint64_t s_full;    // S(j), dP(j) in TMEM            (commit)
   uint64_t sdp_free;  // elementwise read S(j), dP(j)    (8 warps)
   uint64_t ds_full[2];  // dS(j), keys 0-63 / 64-127, in TMEM (4 warps each)
@@ -313,19 +317,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using C = Cfg<DT, D>;
   using BC = BwdCfg<DT, D>;
   constexpr int NS = BC::kSlotsDq;
+  constexpr int NV = NS / 2, NK = NS - NV;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* sbase = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  const uint32_t sQ = smem_u32(sbase), sdO = sQ + C::kTileBytes, sKV = sdO + C::kTileBytes;
-  DqCtrl<NS>* c = reinterpret_cast<DqCtrl<NS>*>(sbase + (2 + NS) * C::kTileBytes);
+  const uint32_t sQ = smem_u32(sbase), sdO = sQ + C::kTileBytes, sK = sdO + C::kTileBytes,
+                 sV = sK + NK * C::kTileBytes;
+  DqCtrl<NK, NV>* c = reinterpret_cast<DqCtrl<NK, NV>*>(sbase + (2 + NS) * C::kTileBytes);
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&c->qd_full), 1);
     mbar_init(smem_u32(&c->qd_empty), 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_u32(&c->kv_full[s]), 1);
-      mbar_init(smem_u32(&c->kv_empty[s]), 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(smem_u32(&c->k_full[s]), 1);
+      mbar_init(smem_u32(&c->k_empty[s]), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(smem_u32(&c->v_full[s]), 1);
+      mbar_init(smem_u32(&c->v_empty[s]), 1);
     }
     mbar_init(smem_u32(&c->s_full), 1);
     mbar_init(smem_u32(&c->sdp_free), 8);
@@ -352,9 +362,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBwdRegsControl));
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t qd_uses = 0, loads = 0, round = 0;
-    int slot = 0;
+    uint32_t qd_uses = 0, loads[2] = {0, 0}, round[2] = {0, 0};
+    int slot[2] = {0, 0};
     bool ok = true;
+    // the next tile of ring kv (0: K, 1: V) once its slot is free
+    auto load_ring = [&](int kv, int j, int bh) -> bool {
+      const int s = slot[kv];
+      const uint32_t empty = smem_u32(kv == 0 ? &c->k_empty[s] : &c->v_empty[s]);
+      const uint32_t full = smem_u32(kv == 0 ? &c->k_full[s] : &c->v_full[s]);
+      if (!wait_bar(empty, (round[kv] & 1u) ^ 1u, wc, 0x42)) return false;
+      mbar_arrive_expect_tx(full, C::kTileBytes);
+      load_tile<DT, D>((kv == 0 ? sK : sV) + s * C::kTileBytes, kv == 0 ? &tmK : &tmV, j * kBlock,
+                       bh, full);
+      ++loads[kv];
+      if (++slot[kv] == (kv == 0 ? NK : NV)) {
+        slot[kv] = 0;
+        ++round[kv];
+      }
+      return true;
+    };
     for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
       const int it = round_item(rnd, p.n_items);
       if (it < 0) continue;
@@ -364,41 +390,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       load_tile<DT, D>(sQ, &tmQ, w.tile * kBlock, w.bh, smem_u32(&c->qd_full));
       load_tile<DT, D>(sdO, &tmdO, w.tile * kBlock, w.bh, smem_u32(&c->qd_full));
       ++qd_uses;
-      for (int j = 0; j < w.n && ok; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          if (!wait_bar(smem_u32(&c->kv_empty[slot]), (round & 1u) ^ 1u, wc, 0x42)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(smem_u32(&c->kv_full[slot]), C::kTileBytes);
-          load_tile<DT, D>(sKV + slot * C::kTileBytes, kv == 0 ? &tmK : &tmV, j * kBlock, w.bh,
-                           smem_u32(&c->kv_full[slot]));
-          ++loads;
-          if (++slot == NS) {
-            slot = 0;
-            ++round;
-          }
-        }
-      }
+      for (int j = 0; j < w.n && ok; ++j) ok = load_ring(0, j, w.bh) && load_ring(1, j, w.bh);
     }
     volatile uint32_t never = 0;
     const WaitCtx wn{&never, p.timeout_ns, p.status, p.where};
-    for (int s = 0; s < NS; ++s) {
-      const uint32_t uses = loads / NS + (static_cast<uint32_t>(s) < loads % NS ? 1u : 0u);
-      if (uses) wait_bar(smem_u32(&c->kv_full[s]), (uses - 1u) & 1u, wn, 0x43);
+    for (int s = 0; s < NK; ++s) {
+      const uint32_t uses = loads[0] / NK + (static_cast<uint32_t>(s) < loads[0] % NK ? 1u : 0u);
+      if (uses) wait_bar(smem_u32(&c->k_full[s]), (uses - 1u) & 1u, wn, 0x43);
+    }
+    for (int s = 0; s < NV; ++s) {
+      const uint32_t uses = loads[1] / NV + (static_cast<uint32_t>(s) < loads[1] % NV ? 1u : 0u);
+      if (uses) wait_bar(smem_u32(&c->v_full[s]), (uses - 1u) & 1u, wn, 0x43);
     }
     if (qd_uses) wait_bar(smem_u32(&c->qd_full), (qd_uses - 1u) & 1u, wn, 0x44);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA
     uint32_t qd_w = 0, sf_w = 0, ds_w = 0, dqe_w = 0;
-    uint32_t round = 0;
-    int slot = 0;
-    auto next_slot = [&](int& s, uint32_t& par) {
-      s = slot;
-      par = round & 1u;
-      if (++slot == NS) {
-        slot = 0;
-        ++round;
+    uint32_t round[2] = {0, 0};
+    int slot[2] = {0, 0};
+    auto next_slot = [&](int kv, int& s, uint32_t& par) {
+      s = slot[kv];
+      par = round[kv] & 1u;
+      if (++slot[kv] == (kv == 0 ? NK : NV)) {
+        slot[kv] = 0;
+        ++round[kv];
       }
     };
     const uint32_t tS = tbase + BC::kDqS, tDP = tbase + BC::kDqDP, tDS = tbase + BC::kDqDS,
@@ -410,35 +425,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const BwdItem w = dq_item<CAUSAL>(it, p);
       int ks, vs;
       uint32_t kp, vp;
-      next_slot(ks, kp);
-      next_slot(vs, vp);
+      next_slot(0, ks, kp);
+      next_slot(1, vs, vp);
       ok = wait_bar(smem_u32(&c->qd_full), qd_w & 1u, wc, 0x51) &&
-           wait_bar(smem_u32(&c->kv_full[ks]), kp, wc, 0x52) &&
-           wait_bar(smem_u32(&c->kv_full[vs]), vp, wc, 0x52);
+           wait_bar(smem_u32(&c->k_full[ks]), kp, wc, 0x52) &&
+           wait_bar(smem_u32(&c->v_full[vs]), vp, wc, 0x52);
       ++qd_w;
       if (!ok) break;
       tc_fence_after_sync();
-      mma_kk<DT, D>(tS, sQ, sKV + ks * C::kTileBytes, BC::kIdescSS);
-      mma_kk<DT, D>(tDP, sdO, sKV + vs * C::kTileBytes, BC::kIdescSS);
+      mma_kk<DT, D>(tS, sQ, sK + ks * C::kTileBytes, BC::kIdescSS);
+      mma_kk<DT, D>(tDP, sdO, sV + vs * C::kTileBytes, BC::kIdescSS);
       mma_commit(smem_u32(&c->s_full));
-      mma_commit(smem_u32(&c->kv_empty[vs]));
+      mma_commit(smem_u32(&c->v_empty[vs]));
       if (w.n == 1) mma_commit(smem_u32(&c->qd_empty));
       for (int j = 0; j < w.n && ok; ++j) {
         const int kcur = ks;
         if (j + 1 < w.n) {
           // S(j+1), dP(j+1) once the elementwise warps have read S(j), dP(j)
-          next_slot(ks, kp);
-          next_slot(vs, vp);
+          next_slot(0, ks, kp);
+          next_slot(1, vs, vp);
           ok = wait_bar(smem_u32(&c->sdp_free), sf_w & 1u, wc, 0x53) &&
-               wait_bar(smem_u32(&c->kv_full[ks]), kp, wc, 0x54) &&
-               wait_bar(smem_u32(&c->kv_full[vs]), vp, wc, 0x54);
+               wait_bar(smem_u32(&c->k_full[ks]), kp, wc, 0x54) &&
+               wait_bar(smem_u32(&c->v_full[vs]), vp, wc, 0x54);
           ++sf_w;
           if (!ok) break;
           tc_fence_after_sync();
-          mma_kk<DT, D>(tS, sQ, sKV + ks * C::kTileBytes, BC::kIdescSS);
-          mma_kk<DT, D>(tDP, sdO, sKV + vs * C::kTileBytes, BC::kIdescSS);
+          mma_kk<DT, D>(tS, sQ, sK + ks * C::kTileBytes, BC::kIdescSS);
+          mma_kk<DT, D>(tDP, sdO, sV + vs * C::kTileBytes, BC::kIdescSS);
           mma_commit(smem_u32(&c->s_full));
-          mma_commit(smem_u32(&c->kv_empty[vs]));
+          mma_commit(smem_u32(&c->v_empty[vs]));
           if (j + 2 == w.n) mma_commit(smem_u32(&c->qd_empty));
         } else {
           // keep the sdp_free phases in step: the last read of the item
@@ -454,14 +469,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (!ok) break;
         tc_fence_after_sync();
-        mma_tmn_half<DT, D, 0>(tDQ, tDS, sKV + kcur * C::kTileBytes, BC::kIdescTS, j > 0);
+        mma_tmn_half<DT, D, 0>(tDQ, tDS, sK + kcur * C::kTileBytes, BC::kIdescTS, j > 0);
         ok = wait_bar(smem_u32(&c->ds_full[1]), ds_w & 1u, wc, 0x58);
         ++ds_w;
         if (!ok) break;
         tc_fence_after_sync();
-        mma_tmn_half<DT, D, 1>(tDQ, tDS, sKV + kcur * C::kTileBytes, BC::kIdescTS, true);
+        mma_tmn_half<DT, D, 1>(tDQ, tDS, sK + kcur * C::kTileBytes, BC::kIdescTS, true);
         mma_commit(smem_u32(&c->ds_free));
-        mma_commit(smem_u32(&c->kv_empty[kcur]));
+        mma_commit(smem_u32(&c->k_empty[kcur]));
         if (j + 1 == w.n) mma_commit(smem_u32(&c->dq_full));
       }
     }
