@@ -430,33 +430,59 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
     }
   };
 
+  // S_t(0) of item w with K_0 in ring slot ks; false when a wait gave up
+  auto issue_s0 = [&](const Item& w, int t, int ks) -> bool {
+    if (!wait_bar(smem_u32(&c->q_full[t]), q_waits[t] & 1u, wc, 0x12)) return false;
+    ++q_waits[t];
+    tc_fence_after_sync();
+    issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes, skv + ks * C::kTileBytes);
+    mma_commit(smem_u32(&c->s_full[t]));
+    if (w.n[t] == 1) mma_commit(smem_u32(&c->q_empty[t]));
+    return true;
+  };
+
+  // One-CTA launches (d = 64, e4m3) issue the next item's S_t(0) right
+  // behind this item's last P_t V, where its K_0 and Q_t are already here:
+  // the tensor pipe runs one thread's MMAs in order, so S_t(0) overwrites
+  // P_t only after that product has read it, and the next item's first
+  // softmax starts without waiting for the rest of this item.  Measured:
+  // +2.6% at d = 64, no change with e4m3, and a loss with the two-CTA
+  // clusters, which keep the plain item start.
+  constexpr bool kEarly = !C::kMulticastKV;
+  bool s0_issued = false;  // S_t(0) of this item went out during the previous one
   for (int rnd = 0; rnd * num_clusters<C::kClusterCTAs>() < p.n_items && ok; ++rnd) {
     const int it = round_cluster_item<C::kClusterCTAs>(rnd, p.n_items);
     if (it < 0) continue;
     const Item w = decode_item<NQT, CAUSAL, C::kClusterCTAs>(it, rank, p);
     const int walk = C::kMulticastKV ? w.blocks : w.nmax;
     if (walk == 0) continue;
-    // S_t(0) for every tile.  Every slot of the cluster item is waited for
-    // and released, with or without query tiles here: the partner CTA's
-    // loads land in this CTA's ring too, and a slot is never released
-    // before its data has arrived.
-    int ks;
-    uint32_t kpar;
-    next_slot(ks, kpar);
-    if (!wait_bar(smem_u32(&c->kv_full[ks]), kpar, wc, 0x11)) break;
-    for (int t = 0; t < NQT && ok && w.work; ++t) {
-      if (!wait_bar(smem_u32(&c->q_full[t]), q_waits[t] & 1u, wc, 0x12)) {
-        ok = false;
+    // the next item this CTA walks (its K_0 follows this item's last V)
+    Item wn;
+    wn.work = false;
+    bool early = false;
+    if constexpr (kEarly) {
+      for (int r2 = rnd + 1; r2 * num_clusters<C::kClusterCTAs>() < p.n_items; ++r2) {
+        const int i2 = round_cluster_item<C::kClusterCTAs>(r2, p.n_items);
+        if (i2 < 0) continue;
+        wn = decode_item<NQT, CAUSAL, C::kClusterCTAs>(i2, rank, p);
+        early = wn.work && wn.nmax > 0;
         break;
       }
-      ++q_waits[t];
-      tc_fence_after_sync();
-      issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes, skv + ks * C::kTileBytes);
-      mma_commit(smem_u32(&c->s_full[t]));
-      if (w.n[t] == 1) mma_commit(smem_u32(&c->q_empty[t]));
     }
-    if (!ok) break;
-    release_slot<C::kMulticastKV>(smem_u32(&c->kv_empty[ks]));
+    if (!s0_issued) {
+      // S_t(0) for every tile.  Every slot of the cluster item is waited
+      // for and released, with or without query tiles here: the partner
+      // CTA's loads land in this CTA's ring too, and a slot is never
+      // released before its data has arrived.
+      int ks;
+      uint32_t kpar;
+      next_slot(ks, kpar);
+      if (!wait_bar(smem_u32(&c->kv_full[ks]), kpar, wc, 0x11)) break;
+      for (int t = 0; t < NQT && ok && w.work; ++t) ok = issue_s0(w, t, ks);
+      if (!ok) break;
+      release_slot<C::kMulticastKV>(smem_u32(&c->kv_empty[ks]));
+    }
+    s0_issued = false;
 
     for (int j = 0; j < walk && ok; ++j) {
       int vs;
@@ -464,10 +490,12 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
       next_slot(vs, vpar);
       if (!wait_bar(smem_u32(&c->kv_full[vs]), vpar, wc, 0x13)) break;
       const bool have_next = j + 1 < walk;
+      const bool ahead = kEarly && !have_next && early;  // the next item's S_t(0)
       int ns = 0;
       uint32_t npar = 0;
       bool k_ready = false;
-      if (have_next) next_slot(ns, npar);
+      bool s0_done[2] = {false, false};
+      if (have_next || ahead) next_slot(ns, npar);
       for (int t = 0; t < NQT && ok; ++t) {
         if (j < w.n[t]) {
           // first key half as soon as its P (and the rescaled O) is
@@ -502,11 +530,28 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
           mma_commit(smem_u32(&c->s_full[t]));
           if (j + 2 == w.n[t]) mma_commit(smem_u32(&c->q_empty[t]));
         }
+        if constexpr (kEarly) {
+          // only where K_0 and Q_t are already here: the other tile's P V
+          // must not wait behind them
+          if (ahead) {
+            if (!k_ready) k_ready = mbar_test_wait(smem_u32(&c->kv_full[ns]), npar);
+            if (k_ready && mbar_test_wait(smem_u32(&c->q_full[t]), q_waits[t] & 1u)) {
+              ok = issue_s0(wn, t, ns);
+              s0_done[t] = true;
+            }
+          }
+        }
       }
       if (!ok) break;
       release_slot<C::kMulticastKV>(smem_u32(&c->kv_empty[vs]));
-      if (have_next) {
+      if (have_next || ahead) {
         if (!k_ready && !wait_bar(smem_u32(&c->kv_full[ns]), npar, wc, 0x16)) break;
+        if constexpr (kEarly) {
+          for (int t = 0; t < NQT && ok && ahead; ++t)
+            if (!s0_done[t]) ok = issue_s0(wn, t, ns);
+          if (!ok) break;
+          s0_issued = ahead;
+        }
         release_slot<C::kMulticastKV>(smem_u32(&c->kv_empty[ns]));
       }
     }
