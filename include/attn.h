@@ -96,7 +96,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * folded into the softmax scale and v_descale is applied to O before the
  * bf16 rounding.  The probabilities are re-quantised to e4m3 (scale 1)
  * for the P.V product; the row sum uses them before that rounding.
- * Source: tekromancy page, section 5 (FP8 E4M3 forward; per-tensor
+ * Source: "Inside FlashAttention-3 & Warp-Specialized CUDA Kernels",
+ * section 5 (FP8 E4M3 forward; per-tensor
  * scaling).  Arguments as attn_fwd with dtype ATTN_FP8_E4M3 (d = 128); the
  * descales must be finite and > 0.
  */
@@ -111,7 +112,8 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
  * tile t is code * scale[bh][t]), as attn_quantize_fp8 produces them, and
  * e4m3 V with one per-tensor descale.  Per key block the softmax uses
  * scale * q_scale[tile] * k_scale[block]; everything else is attn_fwd_fp8.
- * Source: tekromancy page, section 5 (block quantisation of FP8 attention
+ * Source: "Inside FlashAttention-3 & Warp-Specialized CUDA Kernels",
+ * section 5 (block quantisation of FP8 attention
  * inputs).  q_scales and k_scales: device arrays [B * H, ceil(N / 128)],
  * 4-byte aligned, finite and > 0.  Other arguments as attn_fwd_fp8.
  */
@@ -125,9 +127,11 @@ int attn_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* 
  * or K), optionally after the 16 x 16 Walsh-Hadamard rotation of each group
  * of 16 consecutive channels.  The rotation H is orthonormal and symmetric,
  * so rotating both Q and K keeps Q K^T while spreading outlier channels
- * (tekromancy page, section 5).  Per 128-row tile of each (b, h): scale =
- * max|value| / 448 (1 for an all-zero tile), code = e4m3(value / scale)
- * rounded to nearest even.  The butterfly runs h = 1, 2, 4, 8 over pairs
+ * ("Inside FlashAttention-3 & Warp-Specialized CUDA Kernels", section 5).
+ * Per 128-row tile of each (b, h): scale =
+ * max|value| / 448 (1 for an all-zero tile), code = e4m3(value / scale):
+ * the quotient correctly rounded to fp32, then rounded to e4m3 nearest
+ * even, saturating at +-448.  The butterfly runs h = 1, 2, 4, 8 over pairs
  * (i, i + h) as (a + b, a - b) in fp32, then multiplies by 1/4.
  *   x      : input, dtype ATTN_FP32 / ATTN_FP16 / ATTN_BF16, 16-byte aligned.
  *   codes  : [B, H, N, d] e4m3 output, 16-byte aligned.
