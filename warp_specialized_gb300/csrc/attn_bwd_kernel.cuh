@@ -19,8 +19,8 @@
 //   preprocess   D_i and LSE_i * log2(e) per row into a workspace padded to
 //                whole 128-row tiles (padding rows: LSE = +inf, D = 0, so
 //                their probabilities are exactly 0);
-//   dQ kernel    one 128-row query tile per work item, K_j / V_j streamed
-//                through a TMA ring: S = Q K_j^T and dP = dO V_j^T into
+//   dQ kernel    one 128-row query tile per work item, K_j and V_j streamed
+//                through TMA rings of their own: S = Q K_j^T and dP = dO V_j^T into
 //                Tensor Memory, dS written back to its own TMEM columns,
 //                dQ += dS K_j accumulated in TMEM;
 //   dK/dV kernel one 128-key tile per work item, Q_i / dO_i (and the
