@@ -9,15 +9,18 @@ bracketed by a barrier and a device synchronise.  L2 is flushed (a 256 MiB
 write) before every timed step, outside the kernel's events.  The kernel
 time is measured with CUDA events on the launching stream; `value` is the
 whole-job throughput in TFLOP/s (4*B*H*N^2*d FLOPs per step, halved when
-causal), the max over ranks.  With N GPUs (torchrun, one rank per GPU) every
-rank runs its own copy of the workload (independent heads; no exchange), so
-scaling is weak.
+causal), the max over ranks.  With N GPUs every rank runs its own copy of
+the workload (independent heads; no exchange), so scaling is weak.  Under
+torchrun the ranks come from its environment; `--gpus N` without it starts
+the N ranks itself (torch.distributed.run on 127.0.0.1, one rank per GPU).
 
 Also reported: `e2e` (the same metric through the public C-ABI call with the
 inputs copied from pinned host memory and O/LSE copied back every step),
 `roofline` (achieved TFLOP/s of the kernel against the measured dense bf16
-peak), `clocks` (nvidia-smi during the timed region) and `cpu_baseline` (the
-fp64 oracle timed on the host cores on a bounded sample of the workload).
+peak), `clocks` (nvidia-smi during the timed region), `per_config` (at one
+GPU: the causal bf16 and the e4m3 N=8192 d=128 workloads, timed the same way
+after the headline) and `cpu_baseline` (the fp64 oracle timed on the host
+cores on a bounded sample of the workload).
 
 --impl reference times that oracle alone, on the same workload, metric and
 unit (each step a bounded sample of rows), and prints the same JSON line
@@ -55,6 +58,33 @@ def dist_env():
     """(rank, local_rank, world) from the torchrun environment."""
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
             int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_command(nproc: int, argv, port: int):
+    """torch.distributed.run command that re-runs this script as nproc ranks
+    on this node (rendezvous on 127.0.0.1)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={nproc}", "--master-addr", "127.0.0.1", "--master-port",
+            str(port), os.path.abspath(__file__), *argv]
+
+
+def check_world(gpus: int):
+    """None when this process should run as a rank; otherwise the number of
+    ranks to start.  Raises ValueError when a launcher's world size
+    contradicts --gpus."""
+    env = os.environ.get("WORLD_SIZE")
+    if env is None:
+        return gpus if gpus > 1 else None
+    if int(env) != gpus:
+        raise ValueError(f"WORLD_SIZE={env} but --gpus {gpus}")
+    return None
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -173,6 +203,9 @@ def run_gpu(args):
     import warp_specialized_gb300 as ws
 
     rank, local_rank, world = dist_env()
+    if local_rank >= torch.cuda.device_count():
+        raise RuntimeError(f"rank {rank}: local rank {local_rank} but only "
+                           f"{torch.cuda.device_count()} GPU(s) visible")
     if world > 1:
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
@@ -309,6 +342,9 @@ def run_gpu(args):
             raise RuntimeError("watchdog fired during the end-to-end leg")
 
     peak, peak_src = load_peaks()
+    per_config = None
+    if world == 1 and not args.no_per_config:
+        per_config = time_other_configs(ws, dev, peak, stream)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(avg_ms, 4),
@@ -335,10 +371,66 @@ def run_gpu(args):
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
     }
+    if per_config is not None:
+        result["per_config"] = per_config
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     return result, rank, world
+
+
+def time_other_configs(ws, dev, peak: float, stream, steps: int = 10):
+    """CUDA-event TFLOP/s and roofline fraction of the causal bf16 workload
+    and of the e4m3 workload (per-tensor descales, its peak taken as twice
+    the measured bf16 one, the nominal dense ratio), each step after an L2
+    flush, median of `steps`."""
+    import torch
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for name, causal in (("bf16_n8192_d128", True), ("fp8_n8192_d128", False)):
+        inp = ai.workload(name)
+        B, H, N, d = inp.shape
+        q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        sh = stream.cuda_stream
+        lib = ws.load_library()
+        if inp.dtype == "fp8":
+            ds = inp.descale
+            call = lambda: lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(),  # noqa: E731
+                                            o.data_ptr(), lse.data_ptr(), B, H, N, d, inp.scale,
+                                            int(causal), ds["q"], ds["k"], ds["v"], sh)
+            pk, dt = 2.0 * peak, "e4m3"
+        else:
+            call = lambda: ws.attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(),  # noqa: E731
+                                           o.data_ptr(), lse.data_ptr(), B, H, N, d, inp.scale,
+                                           causal, ws.ATTN_BF16, sh)
+            pk, dt = peak, "bf16"
+        for _ in range(3):
+            flush.zero_()
+            if call() != 0:
+                raise RuntimeError(f"{name}: launch failed")
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        if ws.attn_fwd_status() != 0:
+            raise RuntimeError(f"{name}: watchdog fired")
+        med = sorted(ms)[len(ms) // 2]
+        tf = ai.workload_flops(B, H, N, d, causal) / med / 1e9
+        out[f"{name}{'_causal' if causal else ''}"] = {
+            "dtype": dt, "causal": causal, "B": B, "H": H, "N": N, "d": d,
+            "ms_median": round(med, 4), "tflops": round(tf, 1), "peak": pk,
+            "frac": round(tf / pk, 4), "steps": steps,
+            "peak_source": "measured bf16 burst" + (" x 2 (nominal e4m3:bf16 dense ratio)"
+                                                    if dt == "e4m3" else "")}
+        del q, k, v, o, lse
+    return out
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -406,6 +498,22 @@ def run_reference(args):
     return result, rank, world
 
 
+def launch_selftest():
+    """One rank of the launcher check: gloo process group, the max over
+    ranks of (rank + 1), and rank 0 prints the world it saw."""
+    import torch.distributed as dist
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("gloo")
+    m = max_over_ranks(rank + 1.0, world)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps({"launch_selftest": True, "n_gpus": world, "max_over_ranks": m}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -416,9 +524,25 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the causal and e4m3 timings after the headline")
+    ap.add_argument("--launch-selftest", action="store_true",
+                    help="start the ranks, exchange one value over gloo and report; no GPU work")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    try:
+        nproc = check_world(args.gpus)
+    except ValueError as e:
+        ap.error(str(e))
+    if nproc is not None:
+        sys.exit(subprocess.call(launch_command(nproc, sys.argv[1:], free_port())))
+
+    if args.launch_selftest:
+        launch_selftest()
+        return
 
     if args.impl == "reference":
         result, rank, _ = run_reference(args)

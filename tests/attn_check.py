@@ -2,11 +2,11 @@
 inputs and compare with the fp64 oracle, element by element.
 
 Tolerances (O against the fp64 oracle; LSE in natural-log units):
-  fp16 / bf16 / fp32 (tf32 products): max |dO| <= 1e-2, mean |dO| <= 1e-3,
-                                      max |dLSE| <= 1e-3
-  e4m3:                               max |dO| <= 6e-2, max |dLSE| <= 1e-3
+  fp16 / bf16 / fp32: max |dO| <= 1e-2, mean |dO| <= 1e-3, max |dLSE| <= 1e-3
+  e4m3:              max |dO| <= 6e-2, max |dLSE| <= 1e-3
 The 16-bit and e4m3 bounds are the ones the method's target states; fp32
-takes the 16-bit bounds (its products run in tf32).
+takes the 16-bit bounds (it runs in exact fp32 arithmetic on the CUDA
+cores, not on the tensor cores).
 """
 from __future__ import annotations
 

@@ -46,3 +46,49 @@ def test_weak_scaling_value():
     # 2 ranks, 10 steps of 1e12 FLOPs each, slowest rank 4 s -> 5 TFLOP/s
     assert bench.weak_scaling_value(1e12, 10, 2, 4.0) == pytest.approx(5.0)
     assert bench.max_over_ranks(3.0, 1) == 3.0
+
+
+def _bench(args, env_extra=None, timeout=240):
+    import json
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env.update(env_extra or {})
+    r = subprocess.run([sys.executable, bench.__file__, *args], capture_output=True, text=True,
+                       env=env, timeout=timeout)
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return r.returncode, [json.loads(ln) for ln in lines], r.stderr
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """`bench.py --gpus 2` outside a launcher starts two ranks itself (gloo
+    here); rank 0 alone prints, and it saw both."""
+    rc, lines, err = _bench(["--gpus", "2", "--launch-selftest"])
+    assert rc == 0, err[-2000:]
+    assert lines == [{"launch_selftest": True, "n_gpus": 2, "max_over_ranks": 2.0}]
+
+
+def test_gpus_flag_must_match_the_launchers_world():
+    rc, lines, err = _bench(["--gpus", "2", "--launch-selftest"],
+                            {"WORLD_SIZE": "3", "RANK": "0", "LOCAL_RANK": "0"})
+    assert rc != 0 and not lines
+    assert "WORLD_SIZE=3 but --gpus 2" in err
+
+
+def test_check_world():
+    env = dict(os.environ)
+    try:
+        os.environ.pop("WORLD_SIZE", None)
+        assert bench.check_world(1) is None
+        assert bench.check_world(4) == 4
+        os.environ["WORLD_SIZE"] = "4"
+        assert bench.check_world(4) is None
+        with pytest.raises(ValueError):
+            bench.check_world(2)
+    finally:
+        os.environ.clear()
+        os.environ.update(env)
+    cmd = bench.launch_command(8, ["--gpus", "8"], 29511)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=8" in cmd and "127.0.0.1" in cmd and cmd[-2:] == ["--gpus", "8"]

@@ -7,6 +7,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <initializer_list>
 
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
@@ -125,6 +126,11 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   int dev = -1;
   rc = current_device(&dev);
   if (rc != kOk) return rc;
+  if (!on_device(q, dev) || !on_device(k, dev) || !on_device(v, dev) || !on_device(o, dev) ||
+      !on_device(lse, dev))
+    return kErrInvalidArg;
+  if (q_block_scale && (!on_device(q_block_scale, dev) || !on_device(k_block_scale, dev)))
+    return kErrInvalidArg;
   if (!resolve_encode()) return kErrCuda;
 
   LaunchArgs a;
@@ -177,6 +183,10 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
   int dev = -1;
   rc = current_device(&dev);
   if (rc != kOk) return rc;
+  for (const void* ptr : {q, k, v, o, dout, static_cast<const void*>(lse),
+                          static_cast<const void*>(dq), static_cast<const void*>(dk),
+                          static_cast<const void*>(dv), static_cast<const void*>(workspace)})
+    if (!on_device(ptr, dev)) return kErrInvalidArg;
   if (!resolve_encode()) return kErrCuda;
   BwdLaunchArgs a;
   a.q = q;

@@ -85,12 +85,6 @@ constexpr int kThreads = 512;
 constexpr int kBlock = 128;            // query rows per tile = keys per block
 constexpr int kSmemLimit = 232448;     // opt-in shared memory per block on sm_100/sm_103
 constexpr int kMaxSlots = 8;
-// K/V tiles travel as two 64-row halves, one loaded by each CTA of a
-// two-CTA cluster and multicast to both.
-constexpr int kClusterSize = 2;
-constexpr uint16_t kClusterMask = 0x3;
-constexpr int kHalfBlock = kBlock / 2;
-constexpr int kHalfBoxBytes = kHalfBlock * 128;
 
 template <int DT, int D>
 struct Cfg {
@@ -104,12 +98,9 @@ struct Cfg {
   // two query tiles per CTA when both S and O of both fit in Tensor Memory
   // (2 * (128 + D) <= 512 columns) and in shared memory
   static constexpr int kNQT = (D <= 128 && kTileBytes <= 32768) ? 2 : 1;
-  // K/V halves multicast to both CTAs of the cluster (measured: +1% at
-  // d = 128, -2.5% at d = 64, where the coupling of the two CTAs costs
-  // more than the halved L2 reads save)
-  static constexpr bool kMulticastKV = kRowBytes >= 256;
-  // CTAs per cluster: two where they share K/V, else one (plain launch)
-  static constexpr int kClusterCTAs = kMulticastKV ? 2 : 1;
+  // issue the next work item's first S behind this item's last P V
+  // (measured: +2.6% at d = 64; no change with e4m3)
+  static constexpr bool kEarlyS0 = kRowBytes <= 128;
   static constexpr int kMiscBytes = 1024 /*alignment*/ + 512 /*barriers*/ +
                                     2 * kBlock * 4 /*alpha*/ + 2 * 2 * kBlock * 4 /*1/l*/;
   static constexpr int kSlotsFit = (kSmemLimit - kMiscBytes - kNQT * kTileBytes) / kTileBytes;
@@ -141,9 +132,8 @@ struct AttnParams {
   int N;
   int BH;
   int n_qt;       // query tiles per head
-  int n_pairs;    // groups of kNQT query tiles per head (one CTA's share)
-  int n_groups;   // cluster work items per head: two adjacent pairs
-  int n_items;    // BH * n_groups
+  int n_pairs;    // groups of kNQT query tiles per head (one work item each)
+  int n_items;    // BH * n_pairs
   int nkv;        // key blocks per head
   float scale_log2;   // scale * (q, k descales) * log2(e)
   float out_scale;    // v descale (1 for non-fp8)
@@ -158,73 +148,47 @@ struct AttnParams {
   unsigned int* where;
 };
 
-// Work of one CTA for one cluster item.  The two CTAs of a cluster take
-// adjacent pairs of query tiles of the same head (pair 2g + rank) and walk
-// the same key/value blocks together, each loading half of every K/V tile
-// for both; a CTA whose pair lies past the head's end (odd pair count) or
-// that needs fewer blocks (causal) still walks all `blocks`, so that both
-// CTAs use the ring slots in the same order.
+// One work item: kNQT adjacent query tiles of one head, walked over the
+// key/value blocks they need.
 struct Item {
   int bh;
   int qt0;
-  int n[2];    // key blocks of each query tile of this CTA (0: no tile)
+  int n[2];    // key blocks of each query tile (0: no such tile)
   int nmax;
-  int blocks;  // key blocks walked by both CTAs of the cluster
-  bool work;   // this CTA has query tiles in the item
 };
 
 template <int NQT, bool CAUSAL>
-__device__ __forceinline__ int pair_blocks(int pair, const AttnParams& p) {
-  return CAUSAL ? min(pair * NQT + NQT, p.nkv) : p.nkv;
-}
-
-template <int NQT, bool CAUSAL, int CL>
-__device__ __forceinline__ Item decode_item(int it, uint32_t rank, const AttnParams& p) {
+__device__ __forceinline__ Item decode_item(int it, const AttnParams& p) {
   Item r;
-  int group;
+  int pair;
   if (CAUSAL) {  // most blocks first
-    group = p.n_groups - 1 - it / p.BH;
+    pair = p.n_pairs - 1 - it / p.BH;
     r.bh = it % p.BH;
-  } else {
-    r.bh = it / p.n_groups;
-    group = it % p.n_groups;
+  } else {       // head-major, so that a head's K/V stay hot in L2
+    r.bh = it / p.n_pairs;
+    pair = it % p.n_pairs;
   }
-  const int pair = CL * group + static_cast<int>(rank);
-  const int last = min(CL * group + CL - 1, p.n_pairs - 1);
-  r.blocks = pair_blocks<NQT, CAUSAL>(last, p);
-  r.work = pair < p.n_pairs;
   r.qt0 = pair * NQT;
   r.nmax = 0;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int qt = r.qt0 + t;
     const int n = CAUSAL ? min(qt + 1, p.nkv) : p.nkv;
-    r.n[t] = (r.work && t < NQT) ? n : 0;
+    r.n[t] = t < NQT ? n : 0;
     r.nmax = max(r.nmax, r.n[t]);
   }
   return r;
 }
 
-// Static persistent schedule: in round r, worker c of G takes item r*G + c
+// Static persistent schedule: in round r, CTA c of G takes item r*G + c
 // on even rounds and r*G + (G-1-c) on odd ones, so that causal items of
-// decreasing size even out.  round_item: one CTA per worker (the backward
-// kernels); round_cluster_item: one two-CTA cluster per worker.
+// decreasing size even out.
 __device__ __forceinline__ int snake_item(int r, int g, int c, int n_items) {
   const int it = r * g + ((r & 1) ? g - 1 - c : c);
   return it < n_items ? it : -1;
 }
 __device__ __forceinline__ int round_item(int r, int n_items) {
   return snake_item(r, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x), n_items);
-}
-template <int CL>
-__device__ __forceinline__ int round_cluster_item(int r, int n_items) {
-  return snake_item(r, static_cast<int>(gridDim.x) / CL, static_cast<int>(blockIdx.x) / CL,
-                    n_items);
-}
-
-template <int CL>
-__device__ __forceinline__ int num_clusters() {
-  return static_cast<int>(gridDim.x) / CL;
 }
 
 // Shared-memory control block (after the tiles).
@@ -279,7 +243,6 @@ __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                               Ctrl<Cfg<DT, D>::kSlots>* c, const AttnParams& p) {
   using C = Cfg<DT, D>;
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
-  const uint32_t rank = cluster_ctarank();
   const uint8_t* sq = sbase;
   const uint8_t* skv = sbase + C::kNQT * C::kTileBytes;
   uint32_t q_uses[2] = {0, 0};
@@ -288,13 +251,12 @@ __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   uint32_t loads = 0;  // total ring loads issued
   bool ok = true;
 
-  for (int rnd = 0; rnd * num_clusters<C::kClusterCTAs>() < p.n_items && ok; ++rnd) {
-    const int it = round_cluster_item<C::kClusterCTAs>(rnd, p.n_items);
+  for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
+    const int it = round_item(rnd, p.n_items);
     if (it < 0) continue;
-    const Item w = decode_item<C::kNQT, CAUSAL, C::kClusterCTAs>(it, rank, p);
+    const Item w = decode_item<C::kNQT, CAUSAL>(it, p);
 #pragma unroll
     for (int t = 0; t < C::kNQT; ++t) {
-      if (!w.work) break;
       const uint32_t full = smem_u32(&c->q_full[t]);
       if (!wait_bar(smem_u32(&c->q_empty[t]), (q_uses[t] & 1u) ^ 1u, wc, 0x01)) {
         ok = false;
@@ -307,14 +269,8 @@ __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
         tma_load_3d(dst + b * C::kBoxBytes, tmQ, b * C::kBoxInner, (w.qt0 + t) * kBlock, w.bh, full);
       ++q_uses[t];
     }
-    // K_j and V_j.  With multicast this CTA loads rows [64 rank, 64 rank +
-    // 64) of every box for both CTAs of the cluster, so each CTA's "full"
-    // barrier counts the whole tile, and a slot is refilled only when both
-    // CTAs have released it (kv_empty counts both MMA threads).
-    // with multicast both CTAs walk the cluster item's blocks together;
-    // otherwise each walks only the blocks of its own tiles
-    const int walk = C::kMulticastKV ? w.blocks : w.nmax;
-    for (int j = 0; j < walk && ok; ++j) {
+    // K_j and V_j, whole 128-row tiles, alternating through the ring
+    for (int j = 0; j < w.nmax && ok; ++j) {
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
         if (!wait_bar(smem_u32(&c->kv_empty[slot]), (round & 1u) ^ 1u, wc, 0x02)) {
@@ -324,19 +280,10 @@ __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
         const uint32_t full = smem_u32(&c->kv_full[slot]);
         mbar_arrive_expect_tx(full, C::kTileBytes);
         const CUtensorMap* map = kv == 0 ? tmK : tmV;
-        if constexpr (C::kMulticastKV) {
-          const uint32_t dst = smem_u32(skv + slot * C::kTileBytes) + rank * kHalfBoxBytes;
+        const uint32_t dst = smem_u32(skv + slot * C::kTileBytes);
 #pragma unroll
-          for (int b = 0; b < C::kNumBox; ++b)
-            tma_load_3d_multicast(dst + b * C::kBoxBytes, map, b * C::kBoxInner,
-                                  j * kBlock + static_cast<int>(rank) * kHalfBlock, w.bh, full,
-                                  kClusterMask);
-        } else {  // whole 128-row boxes, into this CTA only
-          const uint32_t dst = smem_u32(skv + slot * C::kTileBytes);
-#pragma unroll
-          for (int b = 0; b < C::kNumBox; ++b)
-            tma_load_3d(dst + b * C::kBoxBytes, map, b * C::kBoxInner, j * kBlock, w.bh, full);
-        }
+        for (int b = 0; b < C::kNumBox; ++b)
+          tma_load_3d(dst + b * C::kBoxBytes, map, b * C::kBoxInner, j * kBlock, w.bh, full);
         ++loads;
         if (++slot == C::kSlots) {
           slot = 0;
@@ -397,23 +344,12 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
   }
 }
 
-// Release a K/V ring slot once the MMAs issued so far have read it: to both
-// CTAs of the cluster when the slot is filled by multicast, else locally.
-template <bool MULTICAST>
-__device__ __forceinline__ void release_slot(uint32_t bar) {
-  if constexpr (MULTICAST)
-    mma_commit_multicast(bar, kClusterMask);
-  else
-    mma_commit(bar);
-}
-
 template <int DT, int D, bool CAUSAL>
 __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
                          const AttnParams& p) {
   using C = Cfg<DT, D>;
   constexpr int NQT = C::kNQT;
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
-  const uint32_t rank = cluster_ctarank();
   const uint32_t sq = smem_u32(sbase);
   const uint32_t skv = sq + NQT * C::kTileBytes;
   uint32_t q_waits[2] = {0, 0}, p_waits[2] = {0, 0}, r_waits[2] = {0, 0};
@@ -441,46 +377,41 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
     return true;
   };
 
-  // One-CTA launches (d = 64, e4m3) issue the next item's S_t(0) right
-  // behind this item's last P_t V, where its K_0 and Q_t are already here:
-  // the tensor pipe runs one thread's MMAs in order, so S_t(0) overwrites
-  // P_t only after that product has read it, and the next item's first
-  // softmax starts without waiting for the rest of this item.  Measured:
-  // +2.6% at d = 64, no change with e4m3, and a loss with the two-CTA
-  // clusters, which keep the plain item start.
-  constexpr bool kEarly = !C::kMulticastKV;
+  // The next item's S_t(0) goes out right behind this item's last P_t V,
+  // where its K_0 and Q_t are already here: the tensor pipe runs one
+  // thread's MMAs in order, so S_t(0) overwrites P_t only after that
+  // product has read it, and the next item's first softmax starts without
+  // waiting for the rest of this item.
+  constexpr bool kEarly = C::kEarlyS0;
   bool s0_issued = false;  // S_t(0) of this item went out during the previous one
-  for (int rnd = 0; rnd * num_clusters<C::kClusterCTAs>() < p.n_items && ok; ++rnd) {
-    const int it = round_cluster_item<C::kClusterCTAs>(rnd, p.n_items);
+  for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
+    const int it = round_item(rnd, p.n_items);
     if (it < 0) continue;
-    const Item w = decode_item<NQT, CAUSAL, C::kClusterCTAs>(it, rank, p);
-    const int walk = C::kMulticastKV ? w.blocks : w.nmax;
+    const Item w = decode_item<NQT, CAUSAL>(it, p);
+    const int walk = w.nmax;
     if (walk == 0) continue;
     // the next item this CTA walks (its K_0 follows this item's last V)
     Item wn;
-    wn.work = false;
+    wn.nmax = 0;
     bool early = false;
     if constexpr (kEarly) {
-      for (int r2 = rnd + 1; r2 * num_clusters<C::kClusterCTAs>() < p.n_items; ++r2) {
-        const int i2 = round_cluster_item<C::kClusterCTAs>(r2, p.n_items);
+      for (int r2 = rnd + 1; r2 * static_cast<int>(gridDim.x) < p.n_items; ++r2) {
+        const int i2 = round_item(r2, p.n_items);
         if (i2 < 0) continue;
-        wn = decode_item<NQT, CAUSAL, C::kClusterCTAs>(i2, rank, p);
-        early = wn.work && wn.nmax > 0;
+        wn = decode_item<NQT, CAUSAL>(i2, p);
+        early = wn.nmax > 0;
         break;
       }
     }
     if (!s0_issued) {
-      // S_t(0) for every tile.  Every slot of the cluster item is waited
-      // for and released, with or without query tiles here: the partner
-      // CTA's loads land in this CTA's ring too, and a slot is never
-      // released before its data has arrived.
+      // S_t(0) for every tile
       int ks;
       uint32_t kpar;
       next_slot(ks, kpar);
       if (!wait_bar(smem_u32(&c->kv_full[ks]), kpar, wc, 0x11)) break;
-      for (int t = 0; t < NQT && ok && w.work; ++t) ok = issue_s0(w, t, ks);
+      for (int t = 0; t < NQT && ok; ++t) ok = issue_s0(w, t, ks);
       if (!ok) break;
-      release_slot<C::kMulticastKV>(smem_u32(&c->kv_empty[ks]));
+      mma_commit(smem_u32(&c->kv_empty[ks]));
     }
     s0_issued = false;
 
@@ -543,7 +474,7 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
         }
       }
       if (!ok) break;
-      release_slot<C::kMulticastKV>(smem_u32(&c->kv_empty[vs]));
+      mma_commit(smem_u32(&c->kv_empty[vs]));
       if (have_next || ahead) {
         if (!k_ready && !wait_bar(smem_u32(&c->kv_full[ns]), npar, wc, 0x16)) break;
         if constexpr (kEarly) {
@@ -552,7 +483,7 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
           if (!ok) break;
           s0_issued = ahead;
         }
-        release_slot<C::kMulticastKV>(smem_u32(&c->kv_empty[ns]));
+        mma_commit(smem_u32(&c->kv_empty[ns]));
       }
     }
   }
@@ -691,7 +622,6 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
                              const AttnParams& p) {
   using C = Cfg<DT, D>;
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
-  const uint32_t rank = cluster_ctarank();
   const uint32_t lane = lane_id();
   const uint32_t wq = (threadIdx.x >> 5) & 3u;  // warp quarter = TMEM lane group
   const int r = static_cast<int>(wq * 32u + lane);
@@ -700,11 +630,10 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
   uint32_t s_waits = 0;
   uint32_t iter = 0;
 
-  for (int rnd = 0; rnd * num_clusters<C::kClusterCTAs>() < p.n_items; ++rnd) {
-    const int it = round_cluster_item<C::kClusterCTAs>(rnd, p.n_items);
+  for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items; ++rnd) {
+    const int it = round_item(rnd, p.n_items);
     if (it < 0) continue;
-    const Item w = decode_item<C::kNQT, CAUSAL, C::kClusterCTAs>(it, rank, p);
-    if (!w.work) continue;
+    const Item w = decode_item<C::kNQT, CAUSAL>(it, p);
     const int qt = w.qt0 + t;
     const int n = w.n[t];
     float m_run = -INFINITY;  // subtraction reference (log2 units)
@@ -820,7 +749,6 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, con
   using C = Cfg<DT, D>;
   constexpr int NQT = C::kNQT;
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
-  const uint32_t rank = cluster_ctarank();
   const uint32_t lane = lane_id();
   const uint32_t wq = (threadIdx.x >> 5) & 3u;
   const int r = static_cast<int>(wq * 32u + lane);
@@ -828,11 +756,10 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, con
   uint32_t sc_waits[2] = {0, 0}, o_waits[2] = {0, 0};
   uint32_t iter = 0;
 
-  for (int rnd = 0; rnd * num_clusters<C::kClusterCTAs>() < p.n_items; ++rnd) {
-    const int it = round_cluster_item<C::kClusterCTAs>(rnd, p.n_items);
+  for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items; ++rnd) {
+    const int it = round_item(rnd, p.n_items);
     if (it < 0) continue;
-    const Item w = decode_item<NQT, CAUSAL, C::kClusterCTAs>(it, rank, p);
-    if (!w.work) continue;
+    const Item w = decode_item<NQT, CAUSAL>(it, p);
     for (int j = 0; j < w.nmax; ++j) {
       for (int t = 0; t < NQT; ++t) {
         if (j >= w.n[t]) continue;
@@ -926,8 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(smem_u32(&c->kv_full[s]), 1);
-      // with multicast K/V a slot is free once both CTAs released it
-      mbar_init(smem_u32(&c->kv_empty[s]), C::kMulticastKV ? kClusterSize : 1);
+      mbar_init(smem_u32(&c->kv_empty[s]), 1);
     }
     mbar_init(smem_u32(&c->drain), 1);
     c->abort = 0u;
@@ -944,9 +870,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  // the partner CTA's barriers must be initialised before the first
-  // multicast load or release reaches them
-  cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tbase = c->tmem_base;
 
@@ -977,9 +900,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tbase, C::kTmemCols);
   }
-  // neither CTA leaves while the other may still write into its shared
-  // memory or arrive on its barriers
-  cluster_sync_all();
 }
 
 }  // namespace wsattn

@@ -19,10 +19,9 @@ inline CUtensorMapDataType tensor_map_type(int dt) {
 }
 
 // 3-D view (d, N, B*H) of a dense [B, H, N, d] tensor; the box is one
-// 128-byte swizzle row wide and box_rows high (128 for Q tiles, 64 for the
-// K/V halves each CTA of a cluster loads).  Rows past N inside a head read
-// as zeros (out-of-bounds fill), so a ragged last tile never sees the next
-// head.
+// 128-byte swizzle row wide and box_rows high.  Rows past N inside a head
+// read as zeros (out-of-bounds fill), so a ragged last tile never sees the
+// next head.
 template <int DT, int D>
 inline bool encode_map(const LaunchArgs& a, const void* ptr, int box_rows, CUtensorMap* map) {
   using C = Cfg<DT, D>;
@@ -43,11 +42,11 @@ int launch_instance(const LaunchArgs& a) {
   using C = Cfg<DT, D>;
   auto kern = attn_fwd_kernel<DT, D, CAUSAL>;
   // Per device, once: opt in to the shared memory size, and refuse to run
-  // unless the kernel is launched with exactly 128 registers per thread:
-  // the warpgroups' setmaxnreg split (88 + 168 + 168 + 80) draws on that
-  // pool and could never be satisfied by a smaller one.
+  // unless the kernel is launched with exactly 128 registers per thread
+  // (the warpgroups' setmaxnreg split, 88 + 168 + 168 + 80, draws on that
+  // pool and could never be satisfied by a smaller one) and one CTA fits
+  // on an SM.
   static std::atomic<int> ready[kMaxDevices];
-  static std::atomic<int> max_clusters[kMaxDevices];
   if (a.device < 0 || a.device >= kMaxDevices) return kErrDevice;
   int st = ready[a.device].load(std::memory_order_acquire);
   if (st == 0) {
@@ -61,35 +60,20 @@ int launch_instance(const LaunchArgs& a) {
       cudaGetLastError();
       return kErrCuda;
     }
-    // clusters that can be resident at once (one CTA per SM)
-    int nc = a.num_sms;
-    if (C::kClusterCTAs > 1) {
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeClusterDimension;
-      attr.val.clusterDim.x = C::kClusterCTAs;
-      attr.val.clusterDim.y = 1;
-      attr.val.clusterDim.z = 1;
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(C::kClusterCTAs * a.num_sms, 1, 1);
-      cfg.blockDim = dim3(kThreads, 1, 1);
-      cfg.dynamicSmemBytes = C::kSmemBytes;
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return kErrCuda;
-      }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, C::kSmemBytes) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return kErrCuda;
     }
-    max_clusters[a.device].store(nc, std::memory_order_relaxed);
-    st = (fa.numRegs == 128 && fa.maxThreadsPerBlock >= kThreads && nc >= 1) ? 1 : 2;
+    st = (fa.numRegs == 128 && fa.maxThreadsPerBlock >= kThreads && per_sm >= 1) ? 1 : 2;
     ready[a.device].store(st, std::memory_order_release);
   }
   if (st != 1) return kErrUnsupported;
 
   CUtensorMap mq, mk, mv;
-  const int kv_rows = C::kMulticastKV ? kHalfBlock : kBlock;
-  if (!encode_map<DT, D>(a, a.q, kBlock, &mq) || !encode_map<DT, D>(a, a.k, kv_rows, &mk) ||
-      !encode_map<DT, D>(a, a.v, kv_rows, &mv))
+  if (!encode_map<DT, D>(a, a.q, kBlock, &mq) || !encode_map<DT, D>(a, a.k, kBlock, &mk) ||
+      !encode_map<DT, D>(a, a.v, kBlock, &mv))
     return kErrCuda;
 
   AttnParams p;
@@ -100,8 +84,7 @@ int launch_instance(const LaunchArgs& a) {
   p.n_qt = (a.N + kBlock - 1) / kBlock;
   p.nkv = p.n_qt;
   p.n_pairs = (p.n_qt + C::kNQT - 1) / C::kNQT;
-  p.n_groups = (p.n_pairs + C::kClusterCTAs - 1) / C::kClusterCTAs;
-  p.n_items = p.BH * p.n_groups;
+  p.n_items = p.BH * p.n_pairs;
   p.scale_log2 = a.scale_log2;
   p.out_scale = a.out_scale;
   p.q_block_scale = a.q_block_scale;
@@ -109,20 +92,16 @@ int launch_instance(const LaunchArgs& a) {
   p.timeout_ns = a.timeout_ns;
   p.status = a.status;
   p.where = a.where;
-  const int nc = max_clusters[a.device].load(std::memory_order_relaxed);
-  const int clusters = p.n_items < nc ? p.n_items : nc;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = C::kClusterCTAs;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
+  // persistent grid: one CTA per SM (the shared-memory budget allows no
+  // second), never more CTAs than work items
+  const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C::kClusterCTAs * clusters, 1, 1);
+  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = a.stream;
-  cfg.attrs = &attr;
-  cfg.numAttrs = C::kClusterCTAs > 1 ? 1 : 0;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
   if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) != cudaSuccess) {
     cudaGetLastError();
     return kErrCuda;

@@ -50,6 +50,18 @@ enum : int {
 
 constexpr int kMaxDevices = 64;
 
+// True when p lies in device memory of device `dev`.  Every pointer the
+// kernels read or write through (TMA tensor maps included) must: host
+// memory, managed memory and another GPU's memory are refused.
+inline bool on_device(const void* p, int dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
 struct BwdLaunchArgs {
   const void* q;
   const void* k;

@@ -255,6 +255,8 @@ extern "C" int attn_quantize_fp8(const void* x, void* codes, float* scales, int 
     cudaGetLastError();
     return kErrDevice;
   }
+  if (!on_device(x, dev) || !on_device(codes, dev) || !on_device(scales, dev))
+    return kErrInvalidArg;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (dtype) {
     case ATTN_FP32:

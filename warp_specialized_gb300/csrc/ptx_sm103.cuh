@@ -82,8 +82,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
-// TMA (no multicast): 3-D tile load global -> shared, completion counted
-// on an mbarrier in bytes.
+// TMA: 3-D tile load global -> this CTA's shared memory, completion
+// counted on an mbarrier in bytes.
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint32_t bar) {
@@ -92,34 +92,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4}], [%5];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
-}
-
-// The same load delivered to every CTA of the cluster named in cta_mask, at
-// the same shared-memory offset, each copy signalling the mbarrier at the
-// same offset in its CTA.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* map, int c0,
-                                                      int c1, int c2, uint32_t bar,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// Thread-block clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// every thread of every CTA of the cluster; orders earlier shared-memory
-// writes (barrier initialisation included) before later cluster accesses
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -219,15 +191,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-// Arrive on the mbarrier at offset `bar` in every CTA of cta_mask once all
-// earlier tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 // Instruction descriptor (kind::f16 / tf32 / f8f6f4, dense):
 //   [4,6) D format (1 = f32)   [7,10) A format   [10,13) B format
 //   [15] A major (0 = K)       [16] B major (1 = MN)
@@ -307,10 +270,9 @@ __device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&r)[8
                : "memory");
 }
 
-// Two 64-column loads (columns c .. c+127 of the lane) and one wait: each
-// instruction stays within 64 destination registers.
 // Two 64-column loads (any two TMEM addresses) completed by one wait:
-// r[0..63] from taddr_a, r[64..127] from taddr_b.
+// r[0..63] from taddr_a, r[64..127] from taddr_b.  Each instruction stays
+// within 64 destination registers.
 __device__ __forceinline__ void tmem_ld_2x64_at(uint32_t taddr_a, uint32_t taddr_b,
                                                 uint32_t (&r)[128]) {
   asm volatile(

@@ -40,6 +40,9 @@ def main(argv=None):
     ap.add_argument("--only", default="fwd,bwd,quant")
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--json", default=None, help="also write the results to this file")
+    ap.add_argument("--cases", default=None,
+                    help="forward cases to run, comma-separated workload[:dtype]:mask, e.g. "
+                         "fp8_n8192_d128:nc,outlier_d64:bf16:causal (default: all)")
     args = ap.parse_args(argv)
     parts = set(args.only.split(","))
 
@@ -75,11 +78,20 @@ def main(argv=None):
         print(key, " ".join(f"{k}={v}" for k, v in kw.items()), flush=True)
 
     if "fwd" in parts:
+        wanted = None
+        if args.cases:
+            wanted = set()
+            for c in args.cases.split(","):
+                f = c.split(":")
+                wanted.add((f[0], f[1] if len(f) == 3 else None, f[-1] == "causal"))
         for name, dt in FWD_CASES:
+            masks = [m for m in (False, True) if wanted is None or (name, dt, m) in wanted]
+            if not masks:
+                continue
             inp = ai.workload(name, dt)
             q, k, v = (t.cuda() for t in (inp.q, inp.k, inp.v))
             B, H, N, d = inp.shape
-            for causal in (False, True):
+            for causal in masks:
                 if inp.dtype == "fp8":
                     ds = inp.descale
                     fn = lambda: ws.attn_fwd_fp8(q, k, v, ds["q"], ds["k"], ds["v"],  # noqa: E731
