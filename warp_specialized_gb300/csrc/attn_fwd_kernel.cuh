@@ -106,6 +106,15 @@ struct Cfg {
   static constexpr int kSlotsFit = (kSmemLimit - kMiscBytes - kNQT * kTileBytes) / kTileBytes;
   static constexpr int kSlots = kSlotsFit > kMaxSlots ? kMaxSlots : kSlotsFit;
   static_assert(kSlots >= 2, "the K/V ring needs at least two slots");
+  // Ring stages.  With four or more slots a stage is a pair of slots that
+  // holds V_j and the K tile that follows it in the stream (K_{j+1}, or
+  // K_0 of the next item), filled and released as one: the MMA thread
+  // waits once and releases once per block.  With two slots (d = 256) every
+  // tile is a stage of its own, so that K_{j+1} can load while V_j is used.
+  static constexpr bool kPair = kSlots >= 4;
+  static constexpr int kStages = kPair ? kSlots / 2 : kSlots;
+  static __host__ __device__ constexpr int v_slot(int st) { return kPair ? 2 * st : st; }
+  static __host__ __device__ constexpr int k_slot(int st) { return kPair ? 2 * st + 1 : st; }
   static constexpr int kSmemBytes = kMiscBytes + (kNQT + kSlots) * kTileBytes;
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
   static_assert(kNQT * kTileBytes % 1024 == 0 && kTileBytes % 1024 == 0, "tile alignment");
@@ -191,16 +200,44 @@ __device__ __forceinline__ int round_item(int r, int n_items) {
   return snake_item(r, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x), n_items);
 }
 
+// The item this CTA takes after the one of round rnd, if any.
+template <int NQT, bool CAUSAL>
+__device__ __forceinline__ bool next_item(int rnd, const AttnParams& p, Item& wn) {
+  for (int r2 = rnd + 1; r2 * static_cast<int>(gridDim.x) < p.n_items; ++r2) {
+    const int i2 = round_item(r2, p.n_items);
+    if (i2 < 0) continue;
+    wn = decode_item<NQT, CAUSAL>(i2, p);
+    return true;
+  }
+  return false;
+}
+
+// Position in the K/V ring: stage index and how many times it wrapped.
+struct RingPos {
+  int st = 0;
+  uint32_t round = 0;
+  template <int NST>
+  __device__ __forceinline__ void next(int& s, uint32_t& parity) {
+    s = st;
+    parity = round & 1u;
+    if (++st == NST) {
+      st = 0;
+      ++round;
+    }
+  }
+};
+
 // Shared-memory control block (after the tiles).
 template <int NSLOT>
 struct Ctrl {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[NSLOT], kv_empty[NSLOT];
   uint64_t s_full[2];    // S_t(j) in TMEM            (MMA commit)
-  uint64_t p_full[2][2]; // P_t(j), keys 0-63 / 64-127, in TMEM (4 softmax warps)
+  // P_t(j) keys 0-63 in TMEM and O_t rescaled for block j (4 softmax + 4
+  // correction warps); P_t(j) keys 64-127 in TMEM (4 softmax warps)
+  uint64_t p_full[2][2];
   uint64_t sc_full[2];   // alpha_t(j) in smem        (4 softmax warps)
   uint64_t o_full[2];    // PV_t(j) done              (MMA commit)
-  uint64_t o_ready[2];   // O_t rescaled for block j  (4 correction warps)
   uint64_t drain;        // all MMAs done             (MMA commit)
   uint32_t tmem_base;
   uint32_t abort;        // set when a wait in this CTA ran out
@@ -235,7 +272,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
 }
 
 // ---------------------------------------------------------------------------
-// producer: Q tiles, then K_j and V_j through the ring
+// producer: Q tiles, then the K and V tiles through the ring
 
 template <int DT, int D, bool CAUSAL>
 __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
@@ -244,17 +281,44 @@ __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   using C = Cfg<DT, D>;
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
   const uint8_t* sq = sbase;
-  const uint8_t* skv = sbase + C::kNQT * C::kTileBytes;
+  const uint32_t skv = smem_u32(sbase + C::kNQT * C::kTileBytes);
   uint32_t q_uses[2] = {0, 0};
-  int slot = 0;
-  uint32_t round = 0;
-  uint32_t loads = 0;  // total ring loads issued
+  RingPos ring;
+  uint32_t stages = 0;  // ring stages filled
   bool ok = true;
 
+  // One ring stage: V rows [vrow, vrow + 128) and / or K rows [krow, ...)
+  // of heads vbh / kbh (a negative row: no such tile in this stage).
+  auto fill = [&](int vrow, int vbh, int krow, int kbh) -> bool {
+    int st;
+    uint32_t par;
+    ring.next<C::kStages>(st, par);
+    if (!wait_bar(smem_u32(&c->kv_empty[st]), par ^ 1u, wc, 0x02)) return false;
+    const uint32_t full = smem_u32(&c->kv_full[st]);
+    mbar_arrive_expect_tx(full, ((vrow >= 0) + (krow >= 0)) * C::kTileBytes);
+    if (vrow >= 0) {
+      const uint32_t dst = skv + C::v_slot(st) * C::kTileBytes;
+#pragma unroll
+      for (int b = 0; b < C::kNumBox; ++b)
+        tma_load_3d(dst + b * C::kBoxBytes, tmV, b * C::kBoxInner, vrow, vbh, full);
+    }
+    if (krow >= 0) {
+      const uint32_t dst = skv + C::k_slot(st) * C::kTileBytes;
+#pragma unroll
+      for (int b = 0; b < C::kNumBox; ++b)
+        tma_load_3d(dst + b * C::kBoxBytes, tmK, b * C::kBoxInner, krow, kbh, full);
+    }
+    ++stages;
+    return true;
+  };
+
+  bool k0_loaded = false;  // this item's K_0 went out with the previous item's last V
   for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
     const int it = round_item(rnd, p.n_items);
     if (it < 0) continue;
     const Item w = decode_item<C::kNQT, CAUSAL>(it, p);
+    Item wn;
+    const bool has_next = next_item<C::kNQT, CAUSAL>(rnd, p, wn);
 #pragma unroll
     for (int t = 0; t < C::kNQT; ++t) {
       const uint32_t full = smem_u32(&c->q_full[t]);
@@ -269,37 +333,33 @@ __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
         tma_load_3d(dst + b * C::kBoxBytes, tmQ, b * C::kBoxInner, (w.qt0 + t) * kBlock, w.bh, full);
       ++q_uses[t];
     }
-    // K_j and V_j, whole 128-row tiles, alternating through the ring
-    for (int j = 0; j < w.nmax && ok; ++j) {
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        if (!wait_bar(smem_u32(&c->kv_empty[slot]), (round & 1u) ^ 1u, wc, 0x02)) {
-          ok = false;
-          break;
-        }
-        const uint32_t full = smem_u32(&c->kv_full[slot]);
-        mbar_arrive_expect_tx(full, C::kTileBytes);
-        const CUtensorMap* map = kv == 0 ? tmK : tmV;
-        const uint32_t dst = smem_u32(skv + slot * C::kTileBytes);
-#pragma unroll
-        for (int b = 0; b < C::kNumBox; ++b)
-          tma_load_3d(dst + b * C::kBoxBytes, map, b * C::kBoxInner, j * kBlock, w.bh, full);
-        ++loads;
-        if (++slot == C::kSlots) {
-          slot = 0;
-          ++round;
-        }
+    if constexpr (C::kPair) {
+      // stages (V_j, next K): K_{j+1}, or K_0 of the next item
+      if (ok && !k0_loaded) ok = fill(-1, 0, 0, w.bh);
+      for (int j = 0; j < w.nmax && ok; ++j) {
+        if (j + 1 < w.nmax)
+          ok = fill(j * kBlock, w.bh, (j + 1) * kBlock, w.bh);
+        else
+          ok = fill(j * kBlock, w.bh, has_next ? 0 : -1, has_next ? wn.bh : 0);
+      }
+      k0_loaded = has_next;
+    } else {
+      // one tile per stage: K_j, then V_j
+      for (int j = 0; j < w.nmax && ok; ++j) {
+        ok = fill(-1, 0, j * kBlock, w.bh);
+        if (ok) ok = fill(j * kBlock, w.bh, -1, 0);
       }
     }
   }
-  // Never leave a copy in flight: wait until the last load of every slot
+  // Never leave a copy in flight: wait until the last fill of every stage
   // and of every Q tile has landed (immediate on the normal path).
-  for (int s = 0; s < C::kSlots; ++s) {
-    const uint32_t uses = loads / C::kSlots + (static_cast<uint32_t>(s) < loads % C::kSlots ? 1u : 0u);
+  for (int st = 0; st < C::kStages; ++st) {
+    const uint32_t uses =
+        stages / C::kStages + (static_cast<uint32_t>(st) < stages % C::kStages ? 1u : 0u);
     if (uses) {
       volatile uint32_t never = 0;
       const WaitCtx wc_never{&never, p.timeout_ns, p.status, p.where};
-      wait_bar(smem_u32(&c->kv_full[s]), (uses - 1u) & 1u, wc_never, 0x03);
+      wait_bar(smem_u32(&c->kv_full[st]), (uses - 1u) & 1u, wc_never, 0x03);
     }
   }
   for (int t = 0; t < C::kNQT; ++t) {
@@ -314,15 +374,23 @@ __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 // ---------------------------------------------------------------------------
 // MMA issuer (one thread)
 
+// A shared-memory descriptor moved on by off16 (a byte offset / 16); the
+// start-address field cannot carry into the upper word, since shared
+// addresses stay below 2^18 bytes.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
+  return (d & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(d) + off16);
+}
+
 template <int DT, int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk) {
   using C = Cfg<DT, D>;
+  const uint64_t a0 = make_sdesc_sw128(sq, 16, 1024);
+  const uint64_t b0 = make_sdesc_sw128(sk, 16, 1024);
 #pragma unroll
   for (int k = 0; k < C::kNumQKMma; ++k) {
-    const uint32_t off = (k >> 2) * C::kBoxBytes + (k & 3) * 32;
-    const uint64_t a = make_sdesc_sw128(sq + off, 16, 1024);
-    const uint64_t b = make_sdesc_sw128(sk + off, 16, 1024);
-    mma_ss<C::T::kKind>(d_tmem, a, b, C::kIdescQK, k > 0 ? 1u : 0u);
+    const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
+    mma_ss<C::T::kKind>(d_tmem, desc_add(a0, off), desc_add(b0, off), C::kIdescQK,
+                        k > 0 ? 1u : 0u);
   }
 }
 
@@ -334,13 +402,14 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
   using C = Cfg<DT, D>;
   constexpr int kHalf = C::kNumPVMma / 2;
   static_assert(C::kNumPVMma % 2 == 0, "PV splits into two key halves");
+  // V is [keys, d] with d contiguous: an MN-major B operand.  Each 8-key
+  // group is one 1024-byte swizzle atom (SBO); 128-byte column blocks of d
+  // are one TMA box apart (LBO).
+  const uint64_t b0 = make_sdesc_sw128(sv, C::kBoxBytes, 1024);
 #pragma unroll
   for (int k = HALF * kHalf; k < (HALF + 1) * kHalf; ++k) {
-    // V is [keys, d] with d contiguous: an MN-major B operand.  Each 8-key
-    // group is one 1024-byte swizzle atom (SBO); 128-byte column blocks of d
-    // are one TMA box apart (LBO).
-    const uint64_t b = make_sdesc_sw128(sv + k * C::kKPerMma * 128, C::kBoxBytes, 1024);
-    mma_ts<C::T::kKind>(d_tmem, p_tmem + k * 8, b, C::kIdescPV, (accumulate || k > 0) ? 1u : 0u);
+    mma_ts<C::T::kKind>(d_tmem, p_tmem + k * 8, desc_add(b0, (k * C::kKPerMma * 128) >> 4),
+                        C::kIdescPV, (accumulate || k > 0) ? 1u : 0u);
   }
 }
 
@@ -352,93 +421,78 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
   const uint32_t sq = smem_u32(sbase);
   const uint32_t skv = sq + NQT * C::kTileBytes;
-  uint32_t q_waits[2] = {0, 0}, p_waits[2] = {0, 0}, r_waits[2] = {0, 0};
-  int slot = 0;
-  uint32_t round = 0;
+  uint32_t q_waits[2] = {0, 0}, p_waits[2] = {0, 0};
+  RingPos ring;
   bool ok = true;
 
-  auto next_slot = [&](int& s, uint32_t& par) {
-    s = slot;
-    par = round & 1u;
-    if (++slot == C::kSlots) {
-      slot = 0;
-      ++round;
-    }
-  };
-
-  // S_t(0) of item w with K_0 in ring slot ks; false when a wait gave up
+  // S_t(0) of item w with K_0 in stage ks; false when a wait gave up
   auto issue_s0 = [&](const Item& w, int t, int ks) -> bool {
     if (!wait_bar(smem_u32(&c->q_full[t]), q_waits[t] & 1u, wc, 0x12)) return false;
     ++q_waits[t];
     tc_fence_after_sync();
-    issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes, skv + ks * C::kTileBytes);
+    issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes,
+                    skv + C::k_slot(ks) * C::kTileBytes);
     mma_commit(smem_u32(&c->s_full[t]));
     if (w.n[t] == 1) mma_commit(smem_u32(&c->q_empty[t]));
     return true;
   };
 
-  // The next item's S_t(0) goes out right behind this item's last P_t V,
-  // where its K_0 and Q_t are already here: the tensor pipe runs one
-  // thread's MMAs in order, so S_t(0) overwrites P_t only after that
-  // product has read it, and the next item's first softmax starts without
-  // waiting for the rest of this item.
+  // Where C::kEarlyS0 holds (one-CTA d = 64 and e4m3 launches), the next
+  // item's S_t(0) goes out right behind this item's last P_t V when its
+  // K_0 and Q_t are already here: the tensor pipe runs one thread's MMAs in
+  // order, so S_t(0) overwrites P_t only after that product has read it,
+  // and the next item's first softmax starts without waiting for the rest
+  // of this item.
   constexpr bool kEarly = C::kEarlyS0;
   bool s0_issued = false;  // S_t(0) of this item went out during the previous one
+  int held = -1;           // stage that holds this item's K_0 (paired stages)
   for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
     const int it = round_item(rnd, p.n_items);
     if (it < 0) continue;
     const Item w = decode_item<NQT, CAUSAL>(it, p);
     const int walk = w.nmax;
-    if (walk == 0) continue;
-    // the next item this CTA walks (its K_0 follows this item's last V)
     Item wn;
-    wn.nmax = 0;
-    bool early = false;
-    if constexpr (kEarly) {
-      for (int r2 = rnd + 1; r2 * static_cast<int>(gridDim.x) < p.n_items; ++r2) {
-        const int i2 = round_item(r2, p.n_items);
-        if (i2 < 0) continue;
-        wn = decode_item<NQT, CAUSAL>(i2, p);
-        early = wn.nmax > 0;
-        break;
-      }
-    }
+    const bool has_next = next_item<NQT, CAUSAL>(rnd, p, wn);
     if (!s0_issued) {
       // S_t(0) for every tile
-      int ks;
-      uint32_t kpar;
-      next_slot(ks, kpar);
-      if (!wait_bar(smem_u32(&c->kv_full[ks]), kpar, wc, 0x11)) break;
+      int ks = held;
+      if (ks < 0) {
+        uint32_t kpar;
+        ring.next<C::kStages>(ks, kpar);
+        if (!wait_bar(smem_u32(&c->kv_full[ks]), kpar, wc, 0x11)) break;
+      }
       for (int t = 0; t < NQT && ok; ++t) ok = issue_s0(w, t, ks);
       if (!ok) break;
       mma_commit(smem_u32(&c->kv_empty[ks]));
+      held = -1;
     }
     s0_issued = false;
 
     for (int j = 0; j < walk && ok; ++j) {
       int vs;
       uint32_t vpar;
-      next_slot(vs, vpar);
+      ring.next<C::kStages>(vs, vpar);
       if (!wait_bar(smem_u32(&c->kv_full[vs]), vpar, wc, 0x13)) break;
-      const bool have_next = j + 1 < walk;
-      const bool ahead = kEarly && !have_next && early;  // the next item's S_t(0)
-      int ns = 0;
-      uint32_t npar = 0;
-      bool k_ready = false;
+      const bool last = j + 1 == walk;
+      const bool ahead = kEarly && last && has_next;  // the next item's S_t(0)
+      // stage of the next K: the same one when stages are paired
+      int ns = vs;
+      uint32_t npar = vpar;
+      bool k_ready = C::kPair;
       bool s0_done[2] = {false, false};
-      if (have_next || ahead) next_slot(ns, npar);
+      if (!C::kPair && (!last || ahead)) ring.next<C::kStages>(ns, npar);
+      const uint32_t sv = skv + C::v_slot(vs) * C::kTileBytes;
+      const uint32_t sk = skv + C::k_slot(ns) * C::kTileBytes;
       for (int t = 0; t < NQT && ok; ++t) {
         if (j < w.n[t]) {
-          // first key half as soon as its P (and the rescaled O) is
-          // there, overlapping the softmax of the second half
-          if (!wait_bar(smem_u32(&c->p_full[t][0]), p_waits[t] & 1u, wc, 0x14) ||
-              !wait_bar(smem_u32(&c->o_ready[t]), r_waits[t] & 1u, wc, 0x15)) {
+          // first key half as soon as its P and the rescaled O are there
+          // (p_full[t][0] counts the softmax and the correction warps),
+          // overlapping the softmax of the second half
+          if (!wait_bar(smem_u32(&c->p_full[t][0]), p_waits[t] & 1u, wc, 0x14)) {
             ok = false;
             break;
           }
-          ++r_waits[t];
           tc_fence_after_sync();
-          const uint32_t sv = skv + vs * C::kTileBytes;
           issue_pv_half<DT, D, 0>(tbase + C::o_col(t), tbase + C::s_col(t), sv, j > 0);
           if (!wait_bar(smem_u32(&c->p_full[t][1]), p_waits[t] & 1u, wc, 0x18)) {
             ok = false;
@@ -457,7 +511,7 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
             }
             k_ready = true;
           }
-          issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes, skv + ns * C::kTileBytes);
+          issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes, sk);
           mma_commit(smem_u32(&c->s_full[t]));
           if (j + 2 == w.n[t]) mma_commit(smem_u32(&c->q_empty[t]));
         }
@@ -474,8 +528,8 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
         }
       }
       if (!ok) break;
-      mma_commit(smem_u32(&c->kv_empty[vs]));
-      if (have_next || ahead) {
+      if constexpr (!C::kPair) mma_commit(smem_u32(&c->kv_empty[vs]));
+      if (!last || ahead) {
         if (!k_ready && !wait_bar(smem_u32(&c->kv_full[ns]), npar, wc, 0x16)) break;
         if constexpr (kEarly) {
           for (int t = 0; t < NQT && ok && ahead; ++t)
@@ -484,6 +538,13 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
           s0_issued = ahead;
         }
         mma_commit(smem_u32(&c->kv_empty[ns]));
+      } else if constexpr (C::kPair) {
+        // the last block: this stage also holds the next item's K_0, used
+        // by its S_t(0) before the stage is released
+        if (has_next)
+          held = vs;
+        else
+          mma_commit(smem_u32(&c->kv_empty[vs]));
       }
     }
   }
@@ -795,7 +856,7 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, con
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&c->o_ready[t]));
+        if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t][0]));
       }
     }
     // epilogue: O / l (times the v descale) -> output dtype, row by row
@@ -845,13 +906,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&c->q_full[t]), 1);
       mbar_init(smem_u32(&c->q_empty[t]), 1);
       mbar_init(smem_u32(&c->s_full[t]), 1);
-      mbar_init(smem_u32(&c->p_full[t][0]), 4);
+      mbar_init(smem_u32(&c->p_full[t][0]), 8);
       mbar_init(smem_u32(&c->p_full[t][1]), 4);
       mbar_init(smem_u32(&c->sc_full[t]), 4);
       mbar_init(smem_u32(&c->o_full[t]), 1);
-      mbar_init(smem_u32(&c->o_ready[t]), 4);
     }
-    for (int s = 0; s < C::kSlots; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&c->kv_full[s]), 1);
       mbar_init(smem_u32(&c->kv_empty[s]), 1);
     }
