@@ -284,7 +284,9 @@ __device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&v)[3
   float x[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]) * f;
-  store_out_chunk<DT>(dst, x);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = pack8_out<DT>(x + 8 * i);
 }
 
 // ---------------------------------------------------------------------------

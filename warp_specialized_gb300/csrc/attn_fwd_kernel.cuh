@@ -99,11 +99,13 @@ struct Cfg {
   // (2 * (128 + D) <= 512 columns) and in shared memory
   static constexpr int kNQT = (D <= 128 && kTileBytes <= 32768) ? 2 : 1;
   // issue the next work item's first S behind this item's last P V
-  // (measured: +2.6% at d = 64; no change with e4m3)
-  static constexpr bool kEarlyS0 = kRowBytes <= 128;
+  static constexpr bool kEarlyS0 = true;
   static constexpr int kMiscBytes = 1024 /*alignment*/ + 512 /*barriers*/ +
                                     2 * kBlock * 4 /*alpha*/ + 2 * 2 * kBlock * 4 /*1/l*/;
-  static constexpr int kSlotsFit = (kSmemLimit - kMiscBytes - kNQT * kTileBytes) / kTileBytes;
+  // staging box of the output: 128 rows x 128 bytes (64 columns of 16 bits)
+  static constexpr int kStageBytes = kBlock * 128;
+  static constexpr int kSlotsFit =
+      (kSmemLimit - kMiscBytes - kStageBytes - kNQT * kTileBytes) / kTileBytes;
   static constexpr int kSlots = kSlotsFit > kMaxSlots ? kMaxSlots : kSlotsFit;
   static_assert(kSlots >= 2, "the K/V ring needs at least two slots");
   // Ring stages.  With four or more slots a stage is a pair of slots that
@@ -115,7 +117,7 @@ struct Cfg {
   static constexpr int kStages = kPair ? kSlots / 2 : kSlots;
   static __host__ __device__ constexpr int v_slot(int st) { return kPair ? 2 * st : st; }
   static __host__ __device__ constexpr int k_slot(int st) { return kPair ? 2 * st + 1 : st; }
-  static constexpr int kSmemBytes = kMiscBytes + (kNQT + kSlots) * kTileBytes;
+  static constexpr int kSmemBytes = kMiscBytes + (kNQT + kSlots) * kTileBytes + kStageBytes;
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
   static_assert(kNQT * kTileBytes % 1024 == 0 && kTileBytes % 1024 == 0, "tile alignment");
   static_assert(kRowBytes % 128 == 0, "head dim must fill whole 128-byte swizzle rows");
@@ -237,7 +239,7 @@ struct Ctrl {
   // correction warps); P_t(j) keys 64-127 in TMEM (4 softmax warps)
   uint64_t p_full[2][2];
   uint64_t sc_full[2];   // alpha_t(j) in smem        (4 softmax warps)
-  uint64_t o_full[2];    // PV_t(j) done              (MMA commit)
+  uint64_t o_full[2];    // P_t V of the item's last block done (MMA commit)
   uint64_t drain;        // all MMAs done             (MMA commit)
   uint32_t tmem_base;
   uint32_t abort;        // set when a wait in this CTA ran out
@@ -437,12 +439,11 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
     return true;
   };
 
-  // Where C::kEarlyS0 holds (one-CTA d = 64 and e4m3 launches), the next
-  // item's S_t(0) goes out right behind this item's last P_t V when its
-  // K_0 and Q_t are already here: the tensor pipe runs one thread's MMAs in
-  // order, so S_t(0) overwrites P_t only after that product has read it,
-  // and the next item's first softmax starts without waiting for the rest
-  // of this item.
+  // Where C::kEarlyS0 holds, the next item's S_t(0) goes out right behind
+  // this item's last P_t V when its K_0 and Q_t are already here: the
+  // tensor pipe runs one thread's MMAs in order, so S_t(0) overwrites P_t
+  // only after that product has read it, and the next item's first softmax
+  // starts without waiting for the rest of this item.
   constexpr bool kEarly = C::kEarlyS0;
   bool s0_issued = false;  // S_t(0) of this item went out during the previous one
   int held = -1;           // stage that holds this item's K_0 (paired stages)
@@ -501,7 +502,12 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
           ++p_waits[t];
           tc_fence_after_sync();
           issue_pv_half<DT, D, 1>(tbase + C::o_col(t), tbase + C::s_col(t), sv, true);
-          mma_commit(smem_u32(&c->o_full[t]));
+          // O_t is complete for the epilogue after the tile's last block;
+          // for earlier blocks the correction warps need no signal of their
+          // own: they rescale O_t for block j + 1 only after alpha_t(j + 1),
+          // which the softmax publishes after S_t(j + 1) completed, and that
+          // commit tracks this P_t V too
+          if (j + 1 == w.n[t]) mma_commit(smem_u32(&c->o_full[t]));
         }
         if (j + 1 < w.n[t]) {
           if (!k_ready) {
@@ -781,32 +787,22 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
 // ---------------------------------------------------------------------------
 // correction / epilogue warpgroup
 
+// Eight output values (already scaled) as one 16-byte chunk of the output
+// type (bf16 for e4m3 inputs)
 template <int DT>
-__device__ __forceinline__ void store_out_chunk(void* dst, const float* v);  // 32 values
-
-template <>
-__device__ __forceinline__ void store_out_chunk<1>(void* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    d[i] = make_uint4(pack2<1>(v[8 * i], v[8 * i + 1]), pack2<1>(v[8 * i + 2], v[8 * i + 3]),
-                      pack2<1>(v[8 * i + 4], v[8 * i + 5]), pack2<1>(v[8 * i + 6], v[8 * i + 7]));
-}
-template <>
-__device__ __forceinline__ void store_out_chunk<2>(void* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    d[i] = make_uint4(pack2<2>(v[8 * i], v[8 * i + 1]), pack2<2>(v[8 * i + 2], v[8 * i + 3]),
-                      pack2<2>(v[8 * i + 4], v[8 * i + 5]), pack2<2>(v[8 * i + 6], v[8 * i + 7]));
-}
-template <>
-__device__ __forceinline__ void store_out_chunk<3>(void* dst, const float* v) {
-  store_out_chunk<2>(dst, v);
+__device__ __forceinline__ uint4 pack8_out(const float* v) {
+  constexpr int kOut = DT == 1 ? 1 : 2;
+  return make_uint4(pack2<kOut>(v[0], v[1]), pack2<kOut>(v[2], v[3]), pack2<kOut>(v[4], v[5]),
+                    pack2<kOut>(v[6], v[7]));
 }
 
+// The output is staged through shared memory (one 128-row x 64-column box
+// at a time, in the 128-byte-swizzled layout the O tensor map uses) and
+// written by TMA tensor stores, so that every global write is a whole
+// coalesced box; rows past N are clipped by the tensor map.
 template <int DT, int D, bool CAUSAL>
-__device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, const AttnParams& p) {
+__device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, uint32_t stage,
+                                const CUtensorMap* tmO, const AttnParams& p) {
   using C = Cfg<DT, D>;
   constexpr int NQT = C::kNQT;
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
@@ -814,24 +810,28 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, con
   const uint32_t wq = (threadIdx.x >> 5) & 3u;
   const int r = static_cast<int>(wq * 32u + lane);
   const uint32_t lane_off = (wq * 32u) << 16;
+  const bool issuer = r == 0;  // issues and tracks the TMA stores
+  const uint32_t stage_row = stage + static_cast<uint32_t>(r) * 128u;
   uint32_t sc_waits[2] = {0, 0}, o_waits[2] = {0, 0};
   uint32_t iter = 0;
+  bool ok = true;
 
-  for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items; ++rnd) {
+  for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < p.n_items; ++rnd) {
     const int it = round_item(rnd, p.n_items);
     if (it < 0) continue;
     const Item w = decode_item<NQT, CAUSAL>(it, p);
-    for (int j = 0; j < w.nmax; ++j) {
+    for (int j = 0; j < w.nmax && ok; ++j) {
       for (int t = 0; t < NQT; ++t) {
         if (j >= w.n[t]) continue;
-        if (!wait_bar(smem_u32(&c->sc_full[t]), sc_waits[t] & 1u, wc, 0x31))
-          return;
+        if (!wait_bar(smem_u32(&c->sc_full[t]), sc_waits[t] & 1u, wc, 0x31)) {
+          ok = false;
+          break;
+        }
         ++sc_waits[t];
         const float alpha = c->alpha[t][r];
         if (j > 0) {
-          if (!wait_bar(smem_u32(&c->o_full[t]), o_waits[t] & 1u, wc, 0x32))
-            return;
-          ++o_waits[t];
+          // P_t V_{j-1} has completed: alpha_t(j) was published after
+          // S_t(j), whose commit came after that product
           tc_fence_after_sync();
           // exact skip: a warp whose 32 rows all kept their max has alpha == 1
           if (!__all_sync(0xffffffffu, alpha == 1.0f)) {
@@ -859,28 +859,50 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, con
         if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t][0]));
       }
     }
-    // epilogue: O / l (times the v descale) -> output dtype, row by row
-    for (int t = 0; t < NQT; ++t) {
-      if (!wait_bar(smem_u32(&c->o_full[t]), o_waits[t] & 1u, wc, 0x33)) return;
+    // epilogue: O / l (times the v descale) -> output dtype
+    for (int t = 0; t < NQT && ok; ++t) {
+      if (!wait_bar(smem_u32(&c->o_full[t]), o_waits[t] & 1u, wc, 0x33)) {
+        ok = false;
+        break;
+      }
       ++o_waits[t];
       tc_fence_after_sync();
       const float f = c->inv_l[iter & 1u][t][r] * p.out_scale;
-      const int row = (w.qt0 + t) * kBlock + r;
+      const int qt = w.qt0 + t;
       const uint32_t ta = tbase + lane_off + C::o_col(t);
-      uint8_t* orow = static_cast<uint8_t*>(p.o) +
-                      (static_cast<size_t>(w.bh) * p.N + row) * D * C::T::kOutEsize;
 #pragma unroll 1
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(ta + cc, v);
-        float x[32];
+      for (int bx = 0; bx < D / 64; ++bx) {
+        // the previous store has finished reading the staging box
+        if (issuer) bulk_wait_read_all();
+        named_bar_sync(1, 128);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]) * f;
-        if (row < p.N) store_out_chunk<DT>(orow + cc * C::T::kOutEsize, x);
+        for (int g = 0; g < 2; ++g) {
+          uint32_t v[32];
+          tmem_ld_x32(ta + bx * 64 + g * 32, v);
+          float x[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]) * f;
+          // 16-byte chunk k of the row sits at chunk k ^ (row mod 8)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t k = static_cast<uint32_t>(4 * g + i);
+            st_shared_v4(stage_row + ((k ^ (static_cast<uint32_t>(r) & 7u)) << 4),
+                         pack8_out<DT>(x + 8 * i));
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (issuer && qt * kBlock < p.N) {
+          tma_store_3d(tmO, stage, bx * 64, qt * kBlock, w.bh);
+          bulk_commit_group();
+        }
       }
     }
     ++iter;
   }
+  // no store may still read shared memory (or be in flight) when the CTA
+  // exits
+  if (issuer) bulk_wait_all();
 }
 
 // ---------------------------------------------------------------------------
@@ -888,7 +910,8 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, con
 template <int DT, int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const AttnParams p) {
   using C = Cfg<DT, D>;
   using CtrlT = Ctrl<C::kSlots>;
   static_assert(sizeof(CtrlT) + 1024 <= C::kMiscBytes, "control block budget");
@@ -896,7 +919,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // tiles need 1024-byte alignment (128-byte swizzle atoms)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* sbase = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  CtrlT* c = reinterpret_cast<CtrlT*>(sbase + (C::kNQT + C::kSlots) * C::kTileBytes);
+  const uint32_t stage = smem_u32(sbase + (C::kNQT + C::kSlots) * C::kTileBytes);
+  CtrlT* c = reinterpret_cast<CtrlT*>(sbase + (C::kNQT + C::kSlots) * C::kTileBytes +
+                                      C::kStageBytes);
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
@@ -923,6 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&c->tmem_base), C::kTmemCols);
@@ -950,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (static_cast<int>(wg) - 1 < C::kNQT) role_softmax<DT, D, CAUSAL>(wg - 1, c, tbase, p);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCorrection));
-    role_correction<DT, D, CAUSAL>(c, tbase, p);
+    role_correction<DT, D, CAUSAL>(c, tbase, stage, &tmO, p);
   }
 
   __syncwarp();

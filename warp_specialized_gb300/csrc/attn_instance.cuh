@@ -37,6 +37,23 @@ inline bool encode_map(const LaunchArgs& a, const void* ptr, int box_rows, CUten
   return r == CUDA_SUCCESS;
 }
 
+// The output as the same 3-D view, in its own type (fp16 for fp16 inputs,
+// bf16 otherwise), with boxes of 128 rows x 64 columns: the stores of the
+// epilogue.  Rows past N are never written.
+template <int DT, int D>
+inline bool encode_out_map(const LaunchArgs& a, CUtensorMap* map) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(a.N),
+                        static_cast<cuuint64_t>(a.B) * static_cast<cuuint64_t>(a.H)};
+  cuuint64_t strides[2] = {D * 2ull, static_cast<cuuint64_t>(a.N) * D * 2ull};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kBlock), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = a.encode(map, DT == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        3, a.o, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int DT, int D, bool CAUSAL>
 int launch_instance(const LaunchArgs& a) {
   using C = Cfg<DT, D>;
@@ -71,9 +88,9 @@ int launch_instance(const LaunchArgs& a) {
   }
   if (st != 1) return kErrUnsupported;
 
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!encode_map<DT, D>(a, a.q, kBlock, &mq) || !encode_map<DT, D>(a, a.k, kBlock, &mk) ||
-      !encode_map<DT, D>(a, a.v, kBlock, &mv))
+      !encode_map<DT, D>(a, a.v, kBlock, &mv) || !encode_out_map<DT, D>(a, &mo))
     return kErrCuda;
 
   AttnParams p;
@@ -102,7 +119,7 @@ int launch_instance(const LaunchArgs& a) {
   cfg.stream = a.stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, p) != cudaSuccess) {
     cudaGetLastError();
     return kErrCuda;
   }
