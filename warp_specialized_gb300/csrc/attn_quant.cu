@@ -9,8 +9,9 @@
 // (h = 1, 2, 4, 8: (a, b) -> (a + b, a - b) in fp32, then * 1/4), the
 // block's absolute maximum is reduced over the CTA, scale = amax / 448 (IEEE
 // division; 1 for an all-zero block) and code = e4m3(value / scale), the
-// quotient correctly rounded in fp32, then to e4m3 nearest even, saturating.  HBM-bound: it reads the tensor once and
-// writes one byte per element plus one scale per block.
+// quotient correctly rounded in fp32, then to e4m3 nearest even,
+// saturating.  HBM-bound: it reads the tensor once and writes one byte per
+// element plus one scale per block.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -21,6 +22,7 @@
 
 #include "attn.h"
 #include "attn_launch.h"
+#include "ptx_sm103.cuh"
 
 namespace wsattn {
 namespace {
@@ -64,7 +66,8 @@ __device__ __forceinline__ void unpack_chunk<__half>(const uint4 x, float (&v)[8
 // Stages h = 1, 2, 4, 8 in that order, each (a, b) -> (a + b, a - b) in fp32
 // for the pair (i, i + h): stages below E pair channels inside a lane, the
 // others pair a lane with lane ^ (h / E), where the lane holding i keeps
-// a + b and the lane holding i + h keeps a - b.  Then * 1/4.
+// a + b and the lane holding i + h keeps a - b.  The final * 1/4 is left to
+// the caller (it is exact, and folds into the block scale).
 template <int E>
 __device__ __forceinline__ void wht16_lanes(float (&v)[E]) {
 #pragma unroll
@@ -89,38 +92,48 @@ __device__ __forceinline__ void wht16_lanes(float (&v)[E]) {
       v[i] = __fmaf_rn(sgn, v[i], other);
     }
   }
-#pragma unroll
-  for (int i = 0; i < E; ++i) v[i] = __fmul_rn(v[i], 0.25f);
 }
 
-// value / scale correctly rounded, from y = 1 / scale correctly rounded, by
-// Markstein's refinement (P. Markstein, "Computation of elementary functions
-// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
-// with r = a - q b computed exactly by an fma, RN(q + r y) is the correctly
-// rounded quotient whenever q is within one ulp of a / b.  q = RN(a y) can be
-// off by up to 1.5 ulp, so one refinement first makes it faithful and a
-// second rounds it correctly.  Valid while neither the quotient's ulp times
-// b nor y leaves the normal range: the caller takes this path only for
-// 2^-60 <= scale <= 2^60 with |value| <= 448 scale, where every quotient that
-// can reach a nonzero e4m3 code (|a / b| > 2^-10) has an exact remainder, and
-// smaller ones round to a zero code whatever their last bits; copysign keeps
-// the sign of a zero quotient.
-__device__ __forceinline__ float div_scale(float a, float b, float y) {
-  float q = __fmul_rn(a, y);
-  float r = __fmaf_rn(-q, b, a);
-  q = __fmaf_rn(r, y, q);
-  r = __fmaf_rn(-q, b, a);
-  q = __fmaf_rn(r, y, q);
-  return copysignf(q, a);
-}
-
-// e4m3 codes of one chunk's E values, stored as E bytes
+// e4m3 codes of one chunk's E values, stored as E bytes.
+//
+// With REFINE, value / b is correctly rounded from y = 1 / b correctly
+// rounded by Markstein's refinement (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): with r = a - q b computed exactly by an fma,
+// RN(q + r y) is the correctly rounded quotient whenever q is within one ulp
+// of a / b.  q = RN(a y) can be off by up to 1.5 ulp, so one refinement
+// first makes it faithful and a second rounds it correctly.  Valid while
+// neither the quotient's ulp times b nor y leaves the normal range: the
+// caller takes this path only for 2^-60 <= scale <= 2^60 (b = scale or
+// 4 scale) with |value| <= 448 scale, where every quotient that can reach a
+// nonzero e4m3 code (|a / b| > 2^-10) has an exact remainder, and smaller
+// ones round to a zero code whatever their last bits; copysign keeps the
+// sign of a zero quotient.  The quotients are formed two at a time with
+// the packed f32x2 multiply and fma, each lane rounded exactly as the scalar
+// instruction.
 template <int E, bool REFINE>
-__device__ __forceinline__ void store_codes(const float (&v)[E], float scale, float y,
+__device__ __forceinline__ void store_codes(const float (&v)[E], float b, float y,
                                             uint8_t* dst) {
   float q[E];
+  if constexpr (REFINE) {
+    const uint64_t y2 = f2_pack(y, y);
+    const uint64_t nb2 = f2_pack(-b, -b);
 #pragma unroll
-  for (int i = 0; i < E; ++i) q[i] = REFINE ? div_scale(v[i], scale, y) : __fdiv_rn(v[i], scale);
+    for (int i = 0; i < E; i += 2) {
+      const uint64_t a2 = f2_pack(v[i], v[i + 1]);
+      uint64_t q2 = f2_mul(a2, y2);
+      uint64_t r2 = f2_fma(q2, nb2, a2);
+      q2 = f2_fma(r2, y2, q2);
+      r2 = f2_fma(q2, nb2, a2);
+      q2 = f2_fma(r2, y2, q2);
+      f2_unpack(q2, q[i], q[i + 1]);
+      q[i] = copysignf(q[i], v[i]);
+      q[i + 1] = copysignf(q[i + 1], v[i + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) q[i] = __fdiv_rn(v[i], b);
+  }
   uint32_t pk[E / 4];
 #pragma unroll
   for (int j = 0; j < E / 4; ++j) {
@@ -165,18 +178,44 @@ __global__ void __launch_bounds__(NT) quant_fp8_kernel(const T* __restrict__ x,
 #pragma unroll
   for (int k = 0; k < C; ++k)
     raw[k] = row0 + k * kRowStep < N ? src[k * NT] : make_uint4(0u, 0u, 0u, 0u);
+  // With 16-bit inputs the rotation's exact * 1/4 moves into the divisor:
+  // value / scale = w / (4 scale) for value = w / 4, both exact, since w is
+  // a multiple of the type's smallest step and stays far from fp32's
+  // subnormal floor.  fp32 inputs keep the multiply.
+  constexpr bool kFold = HAD && sizeof(T) == 2;
   float rot[HAD ? C : 1][E];
   float amax = 0.f;
+  if constexpr (!HAD && sizeof(T) == 2) {
+    // |x| of two 16-bit values per word is the word with its sign bits
+    // cleared, and magnitudes order like their bit patterns: the block
+    // maximum is an unsigned 16-bit maximum, two lanes per instruction
+    uint32_t m2 = 0u;
 #pragma unroll
-  for (int k = 0; k < C; ++k) {
-    float v[E];
-    unpack_chunk<T>(raw[k], v);
-    if constexpr (HAD) wht16_lanes<E>(v);
-#pragma unroll
-    for (int i = 0; i < E; ++i) {
-      amax = fmaxf(amax, fabsf(v[i]));
-      if constexpr (HAD) rot[k][i] = v[i];
+    for (int k = 0; k < C; ++k) {
+      m2 = __vmaxu2(m2, raw[k].x & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, raw[k].y & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, raw[k].z & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, raw[k].w & 0x7FFF7FFFu);
     }
+    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    if constexpr (std::is_same<T, __half>::value)
+      amax = __half2float(__ushort_as_half(static_cast<unsigned short>(m)));
+    else
+      amax = __uint_as_float(m << 16);
+  } else {
+#pragma unroll
+    for (int k = 0; k < C; ++k) {
+      float v[E];
+      unpack_chunk<T>(raw[k], v);
+      if constexpr (HAD) {
+        wht16_lanes<E>(v);
+#pragma unroll
+        for (int i = 0; i < E; ++i) rot[k][i] = kFold ? v[i] : __fmul_rn(v[i], 0.25f);
+      }
+#pragma unroll
+      for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(HAD ? rot[k][i] : v[i]));
+    }
+    if constexpr (kFold) amax *= 0.25f;  // the rotated values' maximum
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -187,8 +226,11 @@ __global__ void __launch_bounds__(NT) quant_fp8_kernel(const T* __restrict__ x,
   for (int w = 1; w < NT / 32; ++w) amax = fmaxf(amax, red[w]);
   const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   const bool refine = scale >= 0x1p-60f && scale <= 0x1p60f;  // same for the whole block
-  const float y = __frcp_rn(scale);
   if (threadIdx.x == 0) scales[blk] = scale;
+  // the divisor the codes are formed with (4 scale when the rotation's
+  // * 1/4 is folded in) and its correctly rounded reciprocal
+  const float div = kFold ? scale * 4.0f : scale;
+  const float y = __frcp_rn(div);
   uint8_t* dst = codes + base + static_cast<size_t>(threadIdx.x) * E;
   // one branch for the block, so that the per-element code has none
   auto store_all = [&](auto refine_tag) {
@@ -203,7 +245,7 @@ __global__ void __launch_bounds__(NT) quant_fp8_kernel(const T* __restrict__ x,
       } else {
         unpack_chunk<T>(raw[k], v);
       }
-      store_codes<E, kRefine>(v, scale, y, dst + static_cast<size_t>(k) * NT * E);
+      store_codes<E, kRefine>(v, div, y, dst + static_cast<size_t>(k) * NT * E);
     }
   };
   if (refine)
