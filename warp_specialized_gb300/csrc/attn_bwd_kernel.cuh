@@ -86,11 +86,13 @@ struct BwdCfg {
   // the same with N = 64: one half of the streamed tile's rows as B
   static constexpr uint32_t kIdescSSHalf = make_idesc(C::T::kFmt, C::T::kFmt, false, 64, kBlock);
   static constexpr uint32_t kIdescTS = make_idesc(C::T::kFmt, C::T::kFmt, true, D, kBlock);
-  // TMEM columns, dQ kernel: S | dP | dS (16-bit, 64 columns) | dQ
+  // TMEM columns, dQ kernel: S | dP | dS (16-bit, 64 columns) | dQ | Q
+  // (16-bit, the A operand of S = Q K^T, copied in once per query tile)
   static constexpr uint32_t kDqS = 0, kDqDP = 128, kDqDS = 256, kDqAcc = 320;
+  static constexpr uint32_t kDqQ = kDqAcc + D;
   // TMEM columns, dK/dV kernel: S^T (P^T over it) | dP^T (dS^T over it) | dV | dK
   static constexpr uint32_t kKvS = 0, kKvDP = 128, kKvDV = 256, kKvDK = 256 + D;
-  static_assert(kDqAcc + D <= 512 && kKvDK + D <= 512, "Tensor Memory budget");
+  static_assert(kDqQ + D / 2 <= 512 && kKvDK + D <= 512, "Tensor Memory budget");
 };
 
 struct BwdParams {
@@ -215,6 +217,35 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t sa, uint32_t sb
   for (int k = 0; k < C::kNumQKMma; ++k) {
     const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
     mma_ss<C::T::kKind>(d_tmem, a0 + off, b0 + off, idesc, k > 0 ? 1u : 0u);
+  }
+}
+
+// A 128-row, K-major tile (Q) from shared memory into Tensor Memory, in the
+// layout a tcgen05.mma A operand takes there: row r in lane r, elements
+// (2m, 2m + 1) in column m.  One 32-byte K slice per copy, the slices
+// exactly those an SS MMA would read for each K step.
+template <int DT, int D>
+__device__ __forceinline__ void copy_tile_to_tmem(uint32_t t, uint32_t s) {
+  using C = Cfg<DT, D>;
+  const uint64_t a0 = make_sdesc_sw128(s, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < C::kNumQKMma; ++k) {
+    const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
+    tmem_cp_128x256b(t + k * 8, a0 + off);
+  }
+}
+
+// A x B^T with A (128 rows, K-major) in Tensor Memory and B K-major in
+// shared memory (S = Q K^T with Q copied into TMEM)
+template <int DT, int D>
+__device__ __forceinline__ void mma_tk(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
+                                       uint32_t idesc) {
+  using C = Cfg<DT, D>;
+  const uint64_t b0 = make_sdesc_sw128(sb, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < C::kNumQKMma; ++k) {
+    const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
+    mma_ts<C::T::kKind>(d_tmem, a_tmem + k * 8, b0 + off, idesc, k > 0 ? 1u : 0u);
   }
 }
 
@@ -419,7 +450,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     };
     const uint32_t tS = tbase + BC::kDqS, tDP = tbase + BC::kDqDP, tDS = tbase + BC::kDqDS,
-                   tDQ = tbase + BC::kDqAcc;
+                   tDQ = tbase + BC::kDqAcc, tQ = tbase + BC::kDqQ;
     bool ok = true;
     for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items && ok; ++rnd) {
       const int it = round_item(rnd, p.n_items);
@@ -435,7 +466,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++qd_w;
       if (!ok) break;
       tc_fence_after_sync();
-      mma_kk<DT, D>(tS, sQ, sK + ks * C::kTileBytes, BC::kIdescSS);
+      // Q into Tensor Memory (the previous tile's last S was issued before,
+      // and the tensor pipe runs this thread's operations in order), so
+      // that S = Q K_j^T reads only K_j from shared memory
+      copy_tile_to_tmem<DT, D>(tQ, sQ);
+      mma_tk<DT, D>(tS, tQ, sK + ks * C::kTileBytes, BC::kIdescSS);
       mma_kk<DT, D>(tDP, sdO, sV + vs * C::kTileBytes, BC::kIdescSS);
       mma_commit(smem_u32(&c->s_full));
       mma_commit(smem_u32(&c->v_empty[vs]));
@@ -452,7 +487,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ++sf_w;
           if (!ok) break;
           tc_fence_after_sync();
-          mma_kk<DT, D>(tS, sQ, sK + ks * C::kTileBytes, BC::kIdescSS);
+          mma_tk<DT, D>(tS, tQ, sK + ks * C::kTileBytes, BC::kIdescSS);
           mma_kk<DT, D>(tDP, sdO, sV + vs * C::kTileBytes, BC::kIdescSS);
           mma_commit(smem_u32(&c->s_full));
           mma_commit(smem_u32(&c->v_empty[vs]));

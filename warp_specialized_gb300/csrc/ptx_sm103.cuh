@@ -219,6 +219,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
   }
 }
 
+// Copy of 128 rows x 32 bytes from shared memory (a matrix descriptor, as
+// for an MMA operand) into Tensor Memory at taddr: row r to lane r, the 32
+// bytes to 8 consecutive columns.  Executed in order with the issuing
+// thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
