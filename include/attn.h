@@ -91,6 +91,54 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              struct CUstream_st* stream);
 
 /*
+ * attn_fwd_workspace_size - bytes of device workspace attn_fwd_ws and
+ * attn_fwd_fp8_ws need for head dim d and `dtype` on the current device
+ * (it depends on the device's SM count, not on B, H or N); 0 for
+ * ATTN_FP32, whose kernel takes no workspace, or for an invalid d, dtype
+ * or device.
+ */
+unsigned long long attn_fwd_workspace_size(int d, int dtype);
+
+/*
+ * attn_fwd_split_advised - 1 when attn_fwd_ws's split of the leftover work
+ * is expected to finish sooner than attn_fwd's whole rounds for this shape
+ * on the current device, else 0; also 0 for invalid arguments.  The split
+ * is advised only where the problem is a single partial round (fewer work
+ * items than SMs) and its longest item is longer than a tail CTA's share
+ * plus the split's own cost, both counted in key blocks.  Launches nothing.
+ */
+int attn_fwd_split_advised(int B, int H, int N, int d, int causal, int dtype);
+
+/*
+ * attn_fwd_ws - attn_fwd with a caller workspace, which lets the work that
+ * is left over after whole rounds of one (b, h, query tile pair) item per
+ * SM be split along the key axis: a second launch gives every CTA an
+ * equal share of the leftover items' key blocks, and the partial results
+ * of one query tile are merged with the exact rescaling of the online
+ * softmax (each piece keeps its unnormalised O, row maximum m and row sum
+ * l; the merge takes M = max m, weights exp2(m - M), and divides once).
+ * That merge is the running-maximum rescaling of the "Warp specialization"
+ * concept card, Implementation sketch (the consumer's update of the
+ * running max, the rescale factor and the sum), applied across pieces
+ * instead of across key blocks.  O and LSE are those of attn_fwd up to
+ * floating-point reassociation of the row sums.
+ *   workspace       : device memory, 256-byte aligned, at least
+ *                     attn_fwd_workspace_size(d, dtype) bytes, owned by the
+ *                     caller; its contents need no initialisation and are
+ *                     scratch after the call.  One call at a time may use a
+ *                     given workspace (calls on one stream are ordered).
+ *   workspace_bytes : its size.
+ * Other arguments and errors as attn_fwd; a null or short workspace is
+ * ATTN_ERR_INVALID_ARG, a misaligned one ATTN_ERR_MISALIGNED.  Enqueues up
+ * to two kernels (and a memset when no whole round exists).  ATTN_FP32
+ * ignores the workspace.
+ */
+int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int H, int N, int d, float scale, int causal, int dtype,
+                void* workspace, unsigned long long workspace_bytes,
+                struct CUstream_st* stream);
+
+/*
  * attn_fwd_fp8 - forward pass on e4m3 inputs quantised with per-tensor
  * scales: the real values are code * descale.  q_descale * k_descale is
  * folded into the softmax scale and v_descale is applied to O before the
@@ -105,6 +153,16 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
                  int B, int H, int N, int d, float scale, int causal,
                  float q_descale, float k_descale, float v_descale,
                  struct CUstream_st* stream);
+
+/*
+ * attn_fwd_fp8_ws - attn_fwd_fp8 with the caller workspace of attn_fwd_ws
+ * (same split of the leftover work, same workspace rules).
+ */
+int attn_fwd_fp8_ws(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int N, int d, float scale, int causal,
+                    float q_descale, float k_descale, float v_descale,
+                    void* workspace, unsigned long long workspace_bytes,
+                    struct CUstream_st* stream);
 
 /*
  * attn_fwd_fp8_blockscaled - forward pass on e4m3 Q and K that carry one

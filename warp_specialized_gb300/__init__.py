@@ -18,6 +18,7 @@ __all__ = [
     "load_library", "attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
     "attn_watchdog_selftest", "attn_fwd_raw", "attn_bwd", "attn_bwd_workspace_size",
     "attn_bwd_noalloc", "attn_fwd_fp8_blockscaled", "attn_quantize_fp8", "EXPORTED_SYMBOLS",
+    "attn_fwd_workspace_size", "attn_fwd_ws_raw", "attn_fwd_split_advised",
 ]
 
 ATTN_FP32, ATTN_FP16, ATTN_BF16, ATTN_FP8_E4M3 = 0, 1, 2, 3
@@ -29,7 +30,9 @@ STATUS_NAMES = {
 
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
                     "attn_watchdog_selftest", "attn_bwd", "attn_bwd_workspace_size",
-                    "attn_bwd_noalloc", "attn_fwd_fp8_blockscaled", "attn_quantize_fp8")
+                    "attn_bwd_noalloc", "attn_fwd_fp8_blockscaled", "attn_quantize_fp8",
+                    "attn_fwd_workspace_size", "attn_fwd_ws", "attn_fwd_fp8_ws",
+                    "attn_fwd_split_advised")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -66,13 +69,22 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_fwd.restype = i
         lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, f, f, f, vp]
         lib.attn_fwd_fp8.restype = i
+        u64 = ctypes.c_ulonglong
+        lib.attn_fwd_workspace_size.argtypes = [i, i]
+        lib.attn_fwd_workspace_size.restype = u64
+        lib.attn_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, u64, vp]
+        lib.attn_fwd_ws.restype = i
+        lib.attn_fwd_fp8_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, f, f, f, vp, u64,
+                                        vp]
+        lib.attn_fwd_fp8_ws.restype = i
+        lib.attn_fwd_split_advised.argtypes = [i, i, i, i, i, i]
+        lib.attn_fwd_split_advised.restype = i
         lib.attn_fwd_status.argtypes = [vp]
         lib.attn_fwd_status.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_watchdog_selftest.argtypes = [ctypes.c_uint, vp]
         lib.attn_watchdog_selftest.restype = i
-        u64 = ctypes.c_ulonglong
         lib.attn_bwd_workspace_size.argtypes = [i, i, i]
         lib.attn_bwd_workspace_size.restype = u64
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u64, i, i, i, i, f, i, i,
@@ -119,6 +131,52 @@ def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B
                                    float(scale), int(bool(causal)), int(dtype), stream)
 
 
+def attn_fwd_ws_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int,
+                    H: int, N: int, d: int, scale: float, causal: bool, dtype: int, ws_ptr: int,
+                    ws_bytes: int, stream: int = 0) -> int:
+    """attn_fwd_ws with raw device pointers; returns the status code."""
+    return load_library().attn_fwd_ws(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d,
+                                      float(scale), int(bool(causal)), int(dtype), ws_ptr,
+                                      int(ws_bytes), stream)
+
+
+def attn_fwd_workspace_size(d: int, dtype: int) -> int:
+    """Bytes of workspace the forward's tail launch needs on the current device."""
+    return int(load_library().attn_fwd_workspace_size(int(d), int(dtype)))
+
+
+def attn_fwd_split_advised(B: int, H: int, N: int, d: int, causal: bool, dtype: int) -> bool:
+    """Whether splitting the leftover work (attn_fwd_ws) pays for this shape."""
+    return bool(load_library().attn_fwd_split_advised(int(B), int(H), int(N), int(d),
+                                                      int(bool(causal)), int(dtype)))
+
+
+def _use_split(split_tail, workspace, stream, B, H, N, d, causal, code):
+    if split_tail is False or (workspace is None and isinstance(stream, int)):
+        return False
+    if split_tail is None:
+        return attn_fwd_split_advised(B, H, N, d, causal, code)
+    return True
+
+
+def _workspace(d, code, device, stream, workspace):
+    """The caller's workspace, else a fresh one from torch's allocator on the
+    stream the call runs on (so the allocator does not hand the memory to
+    another stream while the kernels still use it)."""
+    import torch
+    if workspace is not None:
+        if workspace.device != device or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+        return workspace
+    size = attn_fwd_workspace_size(d, code)
+    if size == 0:
+        return None
+    if stream is None:
+        return torch.empty(size, dtype=torch.uint8, device=device)
+    with torch.cuda.stream(stream):
+        return torch.empty(size, dtype=torch.uint8, device=device)
+
+
 def _check_qkv(q, k, v):
     if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
         raise ValueError("q, k, v must share one [B, H, N, d] shape")
@@ -129,12 +187,18 @@ def _check_qkv(q, k, v):
             raise ValueError("q, k, v must be contiguous CUDA tensors")
 
 
-def attn_fwd(q, k, v, scale=None, causal: bool = False, out=None, lse=None, stream=None):
+def attn_fwd(q, k, v, scale=None, causal: bool = False, out=None, lse=None, stream=None,
+             split_tail=None, workspace=None):
     """O, LSE = attention forward of [B, H, N, d] CUDA tensors.
 
     scale defaults to 1/sqrt(d).  out / lse may be given preallocated
     ([B, H, N, d] of q's dtype, [B, H, N] fp32).  Asynchronous on `stream`
-    (default: torch's current stream).  Returns (out, lse)."""
+    (default: torch's current stream).  split_tail: True splits the work
+    left after whole rounds of one item per SM along the keys over the SMs
+    (attn_fwd_ws), False never does, None (default) does where
+    attn_fwd_split_advised says it pays; the split uses a uint8 `workspace`
+    of at least attn_fwd_workspace_size(d, dtype) bytes, else one allocated
+    here.  Returns (out, lse)."""
     import torch
     _check_qkv(q, k, v)
     B, H, N, d = q.shape
@@ -146,16 +210,26 @@ def attn_fwd(q, k, v, scale=None, causal: bool = False, out=None, lse=None, stre
         out = torch.empty((B, H, N, d), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    st = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                      B, H, N, d, scale, causal, code, _stream_handle(stream))
+    ws = None
+    if _use_split(split_tail, workspace, stream, B, H, N, d, causal, code):
+        ws = _workspace(d, code, q.device, stream, workspace)
+    if ws is None:
+        st = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr(), B, H, N, d, scale, causal, code, _stream_handle(stream))
+    else:
+        st = attn_fwd_ws_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr(), B, H, N, d, scale, causal, code, ws.data_ptr(),
+                             ws.numel(), _stream_handle(stream))
     if st != 0:
         raise AttnError(st)
     return out, lse
 
 
 def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, scale=None,
-                 causal: bool = False, out=None, lse=None, stream=None):
-    """Forward pass on e4m3 tensors with per-tensor descales; O is bf16."""
+                 causal: bool = False, out=None, lse=None, stream=None, split_tail=None,
+                 workspace=None):
+    """Forward pass on e4m3 tensors with per-tensor descales; O is bf16.
+    split_tail and workspace as in attn_fwd."""
     import torch
     _check_qkv(q, k, v)
     if q.dtype != torch.float8_e4m3fn:
@@ -167,10 +241,16 @@ def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, 
         out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    st = load_library().attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                     lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
-                                     float(q_descale), float(k_descale), float(v_descale),
-                                     _stream_handle(stream))
+    lib = load_library()
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d,
+            float(scale), int(bool(causal)), float(q_descale), float(k_descale), float(v_descale))
+    ws = None
+    if _use_split(split_tail, workspace, stream, B, H, N, d, causal, ATTN_FP8_E4M3):
+        ws = _workspace(d, ATTN_FP8_E4M3, q.device, stream, workspace)
+    if ws is None:
+        st = lib.attn_fwd_fp8(*args, _stream_handle(stream))
+    else:
+        st = lib.attn_fwd_fp8_ws(*args, ws.data_ptr(), ws.numel(), _stream_handle(stream))
     if st != 0:
         raise AttnError(st, "attn_fwd_fp8")
     return out, lse

@@ -113,12 +113,21 @@ int check_args(const void* q, const void* k, const void* v, const void* o, const
   return kOk;
 }
 
+// Workspace bytes of the forward's tail launch for (d, dtype) on a device
+// with num_sms SMs; 0 where no tail launch exists (exact fp32 path).
+unsigned long long fwd_workspace_size(int num_sms, int d, int dtype) {
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16 && dtype != ATTN_FP8_E4M3) return 0ull;
+  return fwd_workspace_bytes(num_sms, d, fwd_nqt(d, dtype == ATTN_FP8_E4M3 ? 1 : 2));
+}
+
 int run(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
         int d, float scale, int causal, int dtype, float q_descale, float k_descale,
         float v_descale, cudaStream_t stream, const float* q_block_scale = nullptr,
-        const float* k_block_scale = nullptr) {
+        const float* k_block_scale = nullptr, void* workspace = nullptr,
+        unsigned long long workspace_bytes = 0ull) {
   int rc = check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype);
   if (rc != kOk) return rc;
+  if (workspace && !aligned(workspace, 256)) return kErrMisaligned;
   if (!finite_positive(q_descale) || !finite_positive(k_descale) || !finite_positive(v_descale))
     return kErrInvalidArg;
   const double sl2 = static_cast<double>(scale) * q_descale * k_descale * 1.4426950408889634;
@@ -130,6 +139,9 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
       !on_device(lse, dev))
     return kErrInvalidArg;
   if (q_block_scale && (!on_device(q_block_scale, dev) || !on_device(k_block_scale, dev)))
+    return kErrInvalidArg;
+  if (workspace && (!on_device(workspace, dev) ||
+                    workspace_bytes < fwd_workspace_size(g_dev[dev].num_sms, d, dtype)))
     return kErrInvalidArg;
   if (!resolve_encode()) return kErrCuda;
 
@@ -155,6 +167,8 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   a.status = g_dev[dev].status;
   a.where = g_dev[dev].where;
   a.encode = g_encode;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
   switch (dtype) {
     case ATTN_FP32: return launch_fp32(a);
     case ATTN_FP16: return launch_fp16(a);
@@ -260,6 +274,50 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
                  float v_descale, struct CUstream_st* stream) {
   return wsattn::run(q, k, v, o, lse, B, H, N, d, scale, causal, ATTN_FP8_E4M3, q_descale,
                      k_descale, v_descale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+unsigned long long attn_fwd_workspace_size(int d, int dtype) {
+  int dev = -1;
+  if (wsattn::current_device(&dev) != wsattn::kOk) return 0ull;
+  if (d != 64 && d != 128 && d != 256) return 0ull;
+  return wsattn::fwd_workspace_size(wsattn::g_dev[dev].num_sms, d, dtype);
+}
+
+int attn_fwd_split_advised(int B, int H, int N, int d, int causal, int dtype) {
+  if (B < 1 || H < 1 || N < 1 || (causal != 0 && causal != 1)) return 0;
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16 && dtype != ATTN_FP8_E4M3) return 0;
+  if (d != 64 && d != 128 && d != 256) return 0;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > (1LL << 24) || N > (1 << 24) || bh * N > INT_MAX) return 0;
+  int dev = -1;
+  if (wsattn::current_device(&dev) != wsattn::kOk) return 0;
+  const int esize = dtype == ATTN_FP8_E4M3 ? 1 : 2;
+  const int nqt = wsattn::fwd_nqt(d, esize);
+  const int n_qt = (N + 127) / 128;
+  const int n_pairs = (n_qt + nqt - 1) / nqt;
+  const wsattn::TailPlan t =
+      wsattn::plan_tail(static_cast<int>(bh), n_pairs, n_qt, nqt, causal != 0,
+                        wsattn::g_dev[dev].num_sms, wsattn::tail_max_pieces(d, esize));
+  return wsattn::tail_split_pays(t) ? 1 : 0;
+}
+
+int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int N, int d, float scale, int causal, int dtype, void* workspace,
+                unsigned long long workspace_bytes, struct CUstream_st* stream) {
+  if (!workspace) return wsattn::kErrInvalidArg;
+  return wsattn::run(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, 1.0f, 1.0f, 1.0f,
+                     reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, workspace,
+                     workspace_bytes);
+}
+
+int attn_fwd_fp8_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int N, int d, float scale, int causal, float q_descale,
+                    float k_descale, float v_descale, void* workspace,
+                    unsigned long long workspace_bytes, struct CUstream_st* stream) {
+  if (!workspace) return wsattn::kErrInvalidArg;
+  return wsattn::run(q, k, v, o, lse, B, H, N, d, scale, causal, ATTN_FP8_E4M3, q_descale,
+                     k_descale, v_descale, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                     nullptr, workspace, workspace_bytes);
 }
 
 unsigned long long attn_bwd_workspace_size(int B, int H, int N) {

@@ -118,6 +118,11 @@ struct Cfg {
   static __host__ __device__ constexpr int v_slot(int st) { return kPair ? 2 * st : st; }
   static __host__ __device__ constexpr int k_slot(int st) { return kPair ? 2 * st + 1 : st; }
   static constexpr int kSmemBytes = kMiscBytes + (kNQT + kSlots) * kTileBytes + kStageBytes;
+  // a piece's (O, m, l) in the tail launch's workspace: O as [D / 4][128]
+  // float4 (four columns of one row per 16 bytes, the 128 rows of a column
+  // quad contiguous, so that a warp's 16-byte accesses are contiguous),
+  // then m[128], l[128]
+  static constexpr int kPartFloats = kBlock * (D + 2);
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
   static_assert(kNQT * kTileBytes % 1024 == 0 && kTileBytes % 1024 == 0, "tile alignment");
   static_assert(kRowBytes % 128 == 0, "head dim must fill whole 128-byte swizzle rows");
@@ -157,6 +162,16 @@ struct AttnParams {
   // code saying which wait ran out (role * 16 + barrier kind)
   unsigned int* status;
   unsigned int* where;
+  // the tail launch (attn_fwd_tail.cuh): items [tail_start, tail_start +
+  // tail_items) with tail_units key blocks in all, shared out over the grid;
+  // the pieces' flags ([tail_items][2], zeroed before the launch) and
+  // results ([G][2][kNQT] of kPartFloats) in the caller's workspace
+  int tail_start;
+  int tail_items;
+  int tail_ramp;   // extra units of the first tail CTA (see tail_range_start)
+  int tail_units;
+  unsigned int* flags;
+  float* part;
 };
 
 // One work item: kNQT adjacent query tiles of one head, walked over the
@@ -928,6 +943,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tmem_alloc(smem_u32(&c->tmem_base), C::kTmemCols);
     tmem_relinquish();
+  }
+  // the tail launch that follows on the stream counts its pieces in these
+  // words: clear them here rather than in a launch of their own; that
+  // launch may place its CTAs on the SMs this grid leaves (it waits for
+  // this grid's completion before it touches the words)
+  if (p.flags != nullptr) {
+    if (blockIdx.x == 0 && warp == 2)
+      for (int i = static_cast<int>(lane); i < 2 * p.tail_items; i += 32) p.flags[i] = 0u;
+    if (threadIdx.x == 0) griddep_launch_dependents();
   }
   tc_fence_before_sync();
   __syncthreads();

@@ -5,6 +5,7 @@
 #include <atomic>
 
 #include "attn_fwd_kernel.cuh"
+#include "attn_fwd_tail.cuh"
 #include "attn_launch.h"
 
 namespace wsattn {
@@ -54,39 +55,45 @@ inline bool encode_out_map(const LaunchArgs& a, CUtensorMap* map) {
   return r == CUDA_SUCCESS;
 }
 
-template <int DT, int D, bool CAUSAL>
-int launch_instance(const LaunchArgs& a) {
-  using C = Cfg<DT, D>;
-  auto kern = attn_fwd_kernel<DT, D, CAUSAL>;
-  // Per device, once: opt in to the shared memory size, and refuse to run
-  // unless the kernel is launched with exactly 128 registers per thread
-  // (the warpgroups' setmaxnreg split, 88 + 168 + 168 + 80, draws on that
-  // pool and could never be satisfied by a smaller one) and one CTA fits
-  // on an SM.
-  static std::atomic<int> ready[kMaxDevices];
-  if (a.device < 0 || a.device >= kMaxDevices) return kErrDevice;
-  int st = ready[a.device].load(std::memory_order_acquire);
+// Per device, once: opt in to the kernel's shared memory size, and refuse
+// to run unless it is launched with exactly 128 registers per thread (the
+// warpgroups' setmaxnreg split draws on that pool and could never be
+// satisfied by a smaller one) and one CTA fits on an SM.  Returns a status.
+template <typename K>
+inline int prepare_fwd_kernel(K kern, int smem_bytes, int device, std::atomic<int>* ready) {
+  int st = ready[device].load(std::memory_order_acquire);
   if (st == 0) {
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) {
       cudaGetLastError();
       return kErrCuda;
     }
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
         cudaSuccess) {
       cudaGetLastError();
       return kErrCuda;
     }
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, C::kSmemBytes) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes) !=
         cudaSuccess) {
       cudaGetLastError();
       return kErrCuda;
     }
     st = (fa.numRegs == 128 && fa.maxThreadsPerBlock >= kThreads && per_sm >= 1) ? 1 : 2;
-    ready[a.device].store(st, std::memory_order_release);
+    ready[device].store(st, std::memory_order_release);
   }
-  if (st != 1) return kErrUnsupported;
+  return st == 1 ? kOk : kErrUnsupported;
+}
+
+template <int DT, int D, bool CAUSAL>
+int launch_instance(const LaunchArgs& a) {
+  using C = Cfg<DT, D>;
+  auto kern = attn_fwd_kernel<DT, D, CAUSAL>;
+  auto tail_kern = attn_fwd_tail_kernel<DT, D, CAUSAL>;
+  static std::atomic<int> ready[kMaxDevices], ready_tail[kMaxDevices];
+  if (a.device < 0 || a.device >= kMaxDevices) return kErrDevice;
+  int rc = prepare_fwd_kernel(kern, C::kSmemBytes, a.device, ready);
+  if (rc != kOk) return rc;
 
   CUtensorMap mq, mk, mv, mo;
   if (!encode_map<DT, D>(a, a.q, kBlock, &mq) || !encode_map<DT, D>(a, a.k, kBlock, &mk) ||
@@ -109,19 +116,76 @@ int launch_instance(const LaunchArgs& a) {
   p.timeout_ns = a.timeout_ns;
   p.status = a.status;
   p.where = a.where;
+  p.tail_start = p.n_items;
+  p.tail_items = 0;
+  p.tail_ramp = 0;
+  p.tail_units = 0;
+  p.flags = nullptr;
+  p.part = nullptr;
+
+  // With a workspace, the main kernel runs whole rounds of num_sms items
+  // and the tail launch the rest; without one, one launch runs all items.
+  const int n_all = p.n_items;
+  const TailPlan plan =
+      a.workspace ? plan_tail(p.BH, p.n_pairs, p.nkv, C::kNQT, CAUSAL, a.num_sms,
+                              tail_max_pieces(D, C::kEsize))
+                  : TailPlan{};
+  const int tail = plan.items;
+  const int tail_grid = plan.grid;
+  if (tail > 0) {
+    rc = prepare_fwd_kernel(tail_kern, TailCfg<DT, D>::kSmemBytes, a.device, ready_tail);
+    if (rc != kOk) return rc;
+    if (a.workspace_bytes < fwd_workspace_bytes(a.num_sms, D, C::kNQT)) return kErrInvalidArg;
+    p.tail_start = plan.start;
+    p.tail_items = tail;
+    p.tail_units = static_cast<int>(plan.units);
+    p.tail_ramp = tail_ramp(plan, plan.start > 0);
+    p.flags = static_cast<unsigned int*>(a.workspace);
+    p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) +
+                                      fwd_flags_bytes(a.num_sms));
+    p.n_items = p.tail_start;
+    // the main launch clears the flags itself; without one, a memset does
+    if (p.n_items == 0 &&
+        cudaMemsetAsync(p.flags, 0, static_cast<size_t>(tail) * 2 * sizeof(unsigned int),
+                        a.stream) != cudaSuccess) {
+      cudaGetLastError();
+      return kErrCuda;
+    }
+  }
   // persistent grid: one CTA per SM (the shared-memory budget allows no
   // second), never more CTAs than work items
-  const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = a.stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
-  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, p) != cudaSuccess) {
-    cudaGetLastError();
-    return kErrCuda;
+  if (p.n_items > 0) {
+    const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = a.stream;
+    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, p) != cudaSuccess) {
+      cudaGetLastError();
+      return kErrCuda;
+    }
+  }
+  if (tail > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tail_grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = TailCfg<DT, D>::kSmemBytes;
+    cfg.stream = a.stream;
+    // behind a main launch, the tail CTAs take the SMs its CTAs leave
+    // without waiting for the last of them (programmatic dependent launch;
+    // the tail kernel waits for the main grid before it reads the flags)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (p.n_items > 0) {
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, tail_kern, mq, mk, mv, mo, p) != cudaSuccess) {
+      cudaGetLastError();
+      return kErrCuda;
+    }
   }
   return kOk;
 }

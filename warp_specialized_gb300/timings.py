@@ -43,6 +43,8 @@ def main(argv=None):
     ap.add_argument("--cases", default=None,
                     help="forward cases to run, comma-separated workload[:dtype]:mask, e.g. "
                          "fp8_n8192_d128:nc,outlier_d64:bf16:causal (default: all)")
+    ap.add_argument("--split", choices=["auto", "on", "off"], default="auto",
+                    help="the forward's split tail launch: where it pays (auto), always, never")
     args = ap.parse_args(argv)
     parts = set(args.only.split(","))
 
@@ -91,18 +93,29 @@ def main(argv=None):
             inp = ai.workload(name, dt)
             q, k, v = (t.cuda() for t in (inp.q, inp.k, inp.v))
             B, H, N, d = inp.shape
+            split = {"auto": None, "on": True, "off": False}[args.split]
+            wsp = None
+            if split is not False:
+                code = ws.ATTN_FP8_E4M3 if inp.dtype == "fp8" else ws.ATTN_BF16
+                wsp = torch.empty(ws.attn_fwd_workspace_size(d, code), dtype=torch.uint8,
+                                  device="cuda")
+            o = torch.empty((B, H, N, d), dtype=torch.bfloat16 if inp.dtype == "fp8" else q.dtype,
+                            device="cuda")
+            lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
             for causal in masks:
                 if inp.dtype == "fp8":
                     ds = inp.descale
                     fn = lambda: ws.attn_fwd_fp8(q, k, v, ds["q"], ds["k"], ds["v"],  # noqa: E731
-                                                 scale=inp.scale, causal=causal)
+                                                 scale=inp.scale, causal=causal, out=o, lse=lse,
+                                                 split_tail=split, workspace=wsp)
                 else:
-                    fn = lambda: ws.attn_fwd(q, k, v, scale=inp.scale, causal=causal)  # noqa: E731
+                    fn = lambda: ws.attn_fwd(q, k, v, scale=inp.scale, causal=causal,  # noqa: E731
+                                             out=o, lse=lse, split_tail=split, workspace=wsp)
                 ms = median_ms(fn)
                 fl = ai.workload_flops(B, H, N, d, causal)
                 record(f"fwd {name}:{inp.dtype}:{'causal' if causal else 'nc'}",
                        ms=round(ms, 4), tflops=round(fl / ms / 1e9, 1))
-            del q, k, v
+            del q, k, v, o, lse, wsp
 
     if "bwd" in parts:
         for name in BWD_CASES:
