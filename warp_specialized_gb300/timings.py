@@ -45,6 +45,9 @@ def main(argv=None):
                          "fp8_n8192_d128:nc,outlier_d64:bf16:causal (default: all)")
     ap.add_argument("--split", choices=["auto", "on", "off"], default="auto",
                     help="the forward's split tail launch: where it pays (auto), always, never")
+    ap.add_argument("--shape", default=None,
+                    help="time only this forward shape B,H,N,d (bf16, N(0,1) inputs, both "
+                         "masks unless --cases names one: e.g. --cases x:nc)")
     args = ap.parse_args(argv)
     parts = set(args.only.split(","))
 
@@ -86,11 +89,21 @@ def main(argv=None):
             for c in args.cases.split(","):
                 f = c.split(":")
                 wanted.add((f[0], f[1] if len(f) == 3 else None, f[-1] == "causal"))
-        for name, dt in FWD_CASES:
+        fwd_cases = FWD_CASES
+        if args.shape:
+            fwd_cases = [("shape", None)]
+            if wanted is not None:
+                wanted = {("shape", None, m) for (_, _, m) in wanted}
+        for name, dt in fwd_cases:
             masks = [m for m in (False, True) if wanted is None or (name, dt, m) in wanted]
             if not masks:
                 continue
-            inp = ai.workload(name, dt)
+            if name == "shape":
+                Bs, Hs, Ns, ds_ = (int(x) for x in args.shape.split(","))
+                inp = ai.make_inputs(Bs, Hs, Ns, ds_, "bf16", seed=11)
+                name = f"B{Bs}_H{Hs}_N{Ns}_d{ds_}"
+            else:
+                inp = ai.workload(name, dt)
             q, k, v = (t.cuda() for t in (inp.q, inp.k, inp.v))
             B, H, N, d = inp.shape
             split = {"auto": None, "on": True, "off": False}[args.split]
