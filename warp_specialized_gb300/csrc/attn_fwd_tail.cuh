@@ -64,7 +64,7 @@ struct TailCfg {
   // the host's restatement of the layout (the tail grid is planned on it)
   static_assert(fwd_region_bytes(D, C::kEsize) == (C::kNQT + C::kSlots) * C::kTileBytes &&
                     fwd_nqt(D, C::kEsize) == C::kNQT && kFwdMiscBytes == C::kMiscBytes &&
-                    kFwdSmemLimit == kSmemLimit && kFwdStageBytes == C::kStageBytes,
+                    kFwdSmemLimit == kSmemLimit && kFwdStageBytes == C::kStageBytes && C::kStageBufs == (C::kEsize == 1 ? 2 : 1),
                 "host copy of the shared-memory layout");
 };
 
@@ -972,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sbase = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t stage = smem_u32(sbase + (C::kNQT + C::kSlots) * C::kTileBytes);
   CtrlT* c = reinterpret_cast<CtrlT*>(sbase + (C::kNQT + C::kSlots) * C::kTileBytes +
-                                      C::kStageBytes);
+                                      C::kStageTotal);
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();

@@ -135,10 +135,10 @@ constexpr int fwd_nqt(int d, int esize) {
 }
 constexpr int fwd_region_bytes(int d, int esize) {
   return (fwd_nqt(d, esize) +
-          ((kFwdSmemLimit - kFwdMiscBytes - kFwdStageBytes -
+          ((kFwdSmemLimit - kFwdMiscBytes - kFwdStageBytes * (esize == 1 ? 2 : 1) -
             fwd_nqt(d, esize) * fwd_tile_bytes(d, esize)) / fwd_tile_bytes(d, esize) > 8
                ? 8
-               : (kFwdSmemLimit - kFwdMiscBytes - kFwdStageBytes -
+               : (kFwdSmemLimit - kFwdMiscBytes - kFwdStageBytes * (esize == 1 ? 2 : 1) -
                   fwd_nqt(d, esize) * fwd_tile_bytes(d, esize)) / fwd_tile_bytes(d, esize))) *
          fwd_tile_bytes(d, esize);
 }
