@@ -69,8 +69,27 @@ int launch_bwd_instance(const BwdLaunchArgs& a) {
   attn_bwd_preprocess_kernel<DT, D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, a.stream>>>(p);
   const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
   kdq<<<grid, kBwdThreads, BC::kSmemDq, a.stream>>>(mq, mk, mv, mdo, p);
-  kdkv<<<grid, kBwdThreads, BC::kSmemDkv, a.stream>>>(mq, mk, mv, mdo, p);
-  return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+  if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+  // The dK/dV kernel reads only what the preprocess kernel (complete before
+  // the dQ kernel started) and the caller wrote, so its CTAs may take the
+  // SMs the dQ kernel's CTAs leave, over the dQ kernel's last round
+  // (programmatic dependent launch); it waits for the dQ grid before it
+  // exits, so that its completion still implies the dQ kernel's.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kBwdThreads, 1, 1);
+  cfg.dynamicSmemBytes = BC::kSmemDkv;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kdkv, mq, mk, mv, mdo, p) != cudaSuccess) {
+    cudaGetLastError();
+    return kErrCuda;
+  }
+  return kOk;
 }
 
 template <int DT, int D>

@@ -385,6 +385,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(smem_u32(&c->tmem_base), 512);
     tmem_relinquish();
   }
+  // the dK/dV grid, which reads nothing this one writes, may take the SMs
+  // this grid's CTAs leave (programmatic dependent launch)
+  if (threadIdx.x == 0) griddep_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -892,6 +895,9 @@ done:
     tc_fence_after_sync();
     tmem_dealloc(tbase, 512);
   }
+  // this grid completes only after the dQ grid before it (a no-op when it
+  // was launched without programmatic serialization)
+  if (threadIdx.x == 0) griddep_wait();
 }
 
 }  // namespace wsattn
