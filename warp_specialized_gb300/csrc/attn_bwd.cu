@@ -66,7 +66,11 @@ int launch_bwd_instance(const BwdLaunchArgs& a) {
   p.where = a.where;
 
   const long long rows = static_cast<long long>(p.BH) * p.Np;
-  attn_bwd_preprocess_kernel<DT, D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, a.stream>>>(p);
+  constexpr int kPreRows = PreprocessShape<D>::kRowsPerBlock;
+  const long long pre_blocks = (rows + kPreRows - 1) / kPreRows;
+  const long long pre_cap = 8LL * a.num_sms;  // eight 256-thread blocks fill an SM
+  attn_bwd_preprocess_kernel<DT, D>
+      <<<static_cast<unsigned>(pre_blocks < pre_cap ? pre_blocks : pre_cap), 256, 0, a.stream>>>(p);
   const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
   kdq<<<grid, kBwdThreads, BC::kSmemDq, a.stream>>>(mq, mk, mv, mdo, p);
   if (cudaGetLastError() != cudaSuccess) return kErrCuda;

@@ -116,32 +116,70 @@ struct BwdParams {
 };
 
 // ---------------------------------------------------------------------------
-// preprocess: one warp per (padded) row
+// preprocess: D / 8 lanes per (padded) row, each reading 16 bytes of O and
+// of dO (a warp holds 256 / D rows), so that every load is a whole 16-byte
+// vector and a warp's loads cover whole rows
 
+template <int D>
+struct PreprocessShape {
+  static constexpr int kLanesPerRow = D / 8;
+  static constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  static constexpr int kRowsPerBlock = 8 * kRowsPerWarp;  // 256 threads
+  static_assert(128 % kRowsPerBlock == 0, "blocks hold whole 128-row tiles");
+};
+
+// One (padded) row: D = dO . O and LSE * log2(e) into the workspace.
 template <int DT, int D>
-__global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const BwdParams p) {
-  using Elem = typename std::conditional<DT == 1, __half, __nv_bfloat16>::type;
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= static_cast<long long>(p.BH) * p.Np) return;
+__device__ __forceinline__ void preprocess_row(const BwdParams& p, long long row, int sub) {
+  using S = PreprocessShape<D>;
   const long long bh = row / p.Np;
   const int i = static_cast<int>(row - bh * p.Np);
-  float2* out = reinterpret_cast<float2*>(p.ws) + row;
-  if (i >= p.N) {
-    if (lane == 0) *out = make_float2(INFINITY, 0.f);
-    return;
+  const bool real = i < p.N;  // padding rows: LSE = +inf, D = 0
+  uint4 ov = make_uint4(0u, 0u, 0u, 0u), dv = ov;
+  float lse = INFINITY;
+  if (real) {  // all three loads in flight together
+    const long long g = (bh * p.N + i) * D + sub * 8;
+    ov = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + g));
+    dv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + g));
+    if (sub == 0) lse = __ldg(p.lse + bh * p.N + i) * 1.4426950408889634f;
   }
-  const long long g = (bh * p.N + i) * D;
-  const Elem* o = static_cast<const Elem*>(p.o) + g;
-  const Elem* dO = static_cast<const Elem*>(p.dout) + g;
+  const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
   float acc = 0.f;
 #pragma unroll
-  for (int c = lane; c < D; c += 32)
-    acc = fmaf(static_cast<float>(o[c]), static_cast<float>(dO[c]), acc);
+  for (int k = 0; k < 4; ++k) {
+    float2 of, df;
+    if constexpr (DT == 1) {
+      of = __half22float2(*reinterpret_cast<const __half2*>(&ow[k]));
+      df = __half22float2(*reinterpret_cast<const __half2*>(&dw[k]));
+    } else {
+      of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[k]));
+      df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[k]));
+    }
+    acc = fmaf(of.x, df.x, acc);
+    acc = fmaf(of.y, df.y, acc);
+  }
+  // the lanes of a row are consecutive and aligned to kLanesPerRow
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0)
-    *out = make_float2(p.lse[bh * p.N + i] * 1.4426950408889634f, acc);
+  for (int off = S::kLanesPerRow / 2; off > 0; off >>= 1)
+    acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (sub == 0) reinterpret_cast<float2*>(p.ws)[row] = make_float2(lse, acc);
+}
+
+// A grid of a few blocks per SM strides over the rows, one row group per
+// warp at a time; the padded row count is a multiple of 128, so every warp
+// step covers whole rows and its shuffles see all 32 lanes.
+template <int DT, int D>
+__global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const BwdParams p) {
+  using S = PreprocessShape<D>;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % S::kLanesPerRow;  // 16-byte column group of the row
+  const long long rows = static_cast<long long>(p.BH) * p.Np;
+  const long long stride = static_cast<long long>(gridDim.x) * S::kRowsPerBlock;
+#pragma unroll 4
+  for (long long row = static_cast<long long>(blockIdx.x) * S::kRowsPerBlock +
+                       (threadIdx.x >> 5) * S::kRowsPerWarp + lane / S::kLanesPerRow;
+       row < rows; row += stride)
+    preprocess_row<DT, D>(p, row, sub);
 }
 
 // ---------------------------------------------------------------------------
