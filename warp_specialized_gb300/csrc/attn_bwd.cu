@@ -42,8 +42,10 @@ int launch_bwd_instance(const BwdLaunchArgs& a) {
   la.d = D;
   la.encode = a.encode;
   CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq64, mdo64;  // the dK/dV kernel streams Q and dO in 64-row halves
   if (!encode_map<DT, D>(la, a.q, kBlock, &mq) || !encode_map<DT, D>(la, a.k, kBlock, &mk) ||
-      !encode_map<DT, D>(la, a.v, kBlock, &mv) || !encode_map<DT, D>(la, a.dout, kBlock, &mdo))
+      !encode_map<DT, D>(la, a.v, kBlock, &mv) || !encode_map<DT, D>(la, a.dout, kBlock, &mdo) ||
+      !encode_map<DT, D>(la, a.q, 64, &mq64) || !encode_map<DT, D>(la, a.dout, 64, &mdo64))
     return kErrCuda;
 
   BwdParams p;
@@ -89,7 +91,7 @@ int launch_bwd_instance(const BwdLaunchArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kdkv, mq, mk, mv, mdo, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kdkv, mq64, mk, mv, mdo64, p) != cudaSuccess) {
     cudaGetLastError();
     return kErrCuda;
   }

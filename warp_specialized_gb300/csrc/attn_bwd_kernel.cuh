@@ -660,7 +660,7 @@ done:
 template <int NST>
 struct DkvCtrl {
   uint64_t kv_full, kv_empty;
-  uint64_t st_full[NST], st_empty[NST];  // stage i: Q_i, dO_i, (lse2, D)_i
+  uint64_t st_full[NST][2], st_empty[NST][2];  // stage i, query half h: Q_i, dO_i, (lse2, D)_i rows 64h .. 64h + 63
   uint64_t s_full[2];  // S^T(i), dP^T(i), queries 0-63 / 64-127, in TMEM (commit)
   uint64_t pds_full[2];  // P^T(i), dS^T(i), queries 0-63 / 64-127, in TMEM (4 warps each)
   uint64_t acc_full;   // last dV / dK MMA of the item done (commit)
@@ -690,8 +690,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&c->kv_full), 1);
     mbar_init(smem_u32(&c->kv_empty), 1);
     for (int s = 0; s < NST; ++s) {
-      mbar_init(smem_u32(&c->st_full[s]), 1);
-      mbar_init(smem_u32(&c->st_empty[s]), 1);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(smem_u32(&c->st_full[s][h]), 1);
+        mbar_init(smem_u32(&c->st_empty[s][h]), 1);
+      }
     }
     mbar_init(smem_u32(&c->s_full[0]), 1);
     mbar_init(smem_u32(&c->s_full[1]), 1);
@@ -731,17 +733,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++kv_uses;
       for (int i = 0; i < w.n; ++i) {
         const int qi = w.first + i;
-        if (!wait_bar(smem_u32(&c->st_empty[st]), (round & 1u) ^ 1u, wc, 0x72)) {
-          ok = false;
-          break;
-        }
-        const uint32_t bar = smem_u32(&c->st_full[st]);
         const uint32_t dst = sSt + st * BC::kStageBytes;
-        mbar_arrive_expect_tx(bar, BC::kStageBytes);
-        load_tile<DT, D>(dst, &tmQ, qi * kBlock, w.bh, bar);
-        load_tile<DT, D>(dst + C::kTileBytes, &tmdO, qi * kBlock, w.bh, bar);
-        bulk_load(dst + 2 * C::kTileBytes,
-                  p.ws + (static_cast<size_t>(w.bh) * p.Np + qi * kBlock) * 2, BC::kVecBytes, bar);
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!wait_bar(smem_u32(&c->st_empty[st][h]), (round & 1u) ^ 1u, wc, 0x72)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&c->st_full[st][h]);
+          mbar_arrive_expect_tx(bar, BC::kStageBytes / 2);
+          // rows 64h .. 64h + 63 of each 128-row box: the bottom half starts at
+          // 8 KiB, a whole number of 1024-byte swizzle atoms, so the bytes are
+          // those of the full box
+#pragma unroll
+          for (int b = 0; b < C::kNumBox; ++b) {
+            tma_load_3d(dst + b * C::kBoxBytes + h * (C::kBoxBytes / 2), &tmQ, b * C::kBoxInner,
+                        qi * kBlock + 64 * h, w.bh, bar);
+            tma_load_3d(dst + C::kTileBytes + b * C::kBoxBytes + h * (C::kBoxBytes / 2), &tmdO,
+                        b * C::kBoxInner, qi * kBlock + 64 * h, w.bh, bar);
+          }
+          bulk_load(dst + 2 * C::kTileBytes + h * (BC::kVecBytes / 2),
+                    p.ws + (static_cast<size_t>(w.bh) * p.Np + qi * kBlock + 64 * h) * 2,
+                    BC::kVecBytes / 2, bar);
+        }
+        if (!ok) break;
         ++loads;
         if (++st == NST) {
           st = 0;
@@ -753,7 +767,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const WaitCtx wn{&never, p.timeout_ns, p.status, p.where};
     for (int s = 0; s < NST; ++s) {
       const uint32_t uses = loads / NST + (static_cast<uint32_t>(s) < loads % NST ? 1u : 0u);
-      if (uses) wait_bar(smem_u32(&c->st_full[s]), (uses - 1u) & 1u, wn, 0x73);
+      for (int h = 0; h < 2 && uses; ++h)
+        wait_bar(smem_u32(&c->st_full[s][h]), (uses - 1u) & 1u, wn, 0x73);
     }
     if (kv_uses) wait_bar(smem_u32(&c->kv_full), (kv_uses - 1u) & 1u, wn, 0x74);
   } else if (warp == 1 && lane == 0) {
@@ -768,7 +783,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (it < 0) continue;
       const BwdItem w = dkv_item<CAUSAL>(it, p);
       ok = wait_bar(smem_u32(&c->kv_full), kv_w & 1u, wc, 0x81) &&
-           wait_bar(smem_u32(&c->st_full[st]), round & 1u, wc, 0x82);
+           wait_bar(smem_u32(&c->st_full[st][0]), round & 1u, wc, 0x82);
       ++kv_w;
       if (!ok) break;
       tc_fence_after_sync();
@@ -791,6 +806,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       {
         const uint32_t sq = sSt + st * BC::kStageBytes;
         issue_sdp(0, sq);
+        if (!wait_bar(smem_u32(&c->st_full[st][1]), round & 1u, wc, 0x82)) break;
+        tc_fence_after_sync();
         issue_sdp(1, sq);
       }
       for (int i = 0; i < w.n && ok; ++i) {
@@ -809,8 +826,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after_sync();
         mma_tmn_part<DT, D, 0>(tDV, tS, sq + C::kTileBytes, BC::kIdescTS, i > 0);
         mma_tmn_part<DT, D, 0>(tDK, tDP, sq, BC::kIdescTS, i > 0);
+        mma_commit(smem_u32(&c->st_empty[st][0]));
         if (have_next) {
-          if (!wait_bar(smem_u32(&c->st_full[nst]), nround & 1u, wc, 0x82)) break;
+          if (!wait_bar(smem_u32(&c->st_full[nst][0]), nround & 1u, wc, 0x82)) break;
+          tc_fence_after_sync();
           issue_sdp(0, sn);
         }
         // queries 64-127
@@ -820,10 +839,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after_sync();
         mma_tmn_part<DT, D, 1>(tDV, tS + 64, sq + C::kTileBytes, BC::kIdescTS, true);
         mma_tmn_part<DT, D, 1>(tDK, tDP + 64, sq, BC::kIdescTS, true);
-        mma_commit(smem_u32(&c->st_empty[st]));
+        mma_commit(smem_u32(&c->st_empty[st][1]));
         st = nst;
         round = nround;
         if (have_next) {
+          if (!wait_bar(smem_u32(&c->st_full[st][1]), round & 1u, wc, 0x82)) break;
+          tc_fence_after_sync();
           issue_sdp(1, sn);
         } else {
           mma_commit(smem_u32(&c->acc_full));
@@ -861,7 +882,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // S^T(i), dP^T(i) in TMEM, and the stage's (lse2, D) rows landed
         // (observed here, not only through the MMA thread)
         if (!wait_bar_all(smem_u32(&c->s_full[half]), sf_w & 1u, wc, 0x91) ||
-            !wait_bar_all(smem_u32(&c->st_full[st]), round & 1u, wc, 0x93))
+            !wait_bar_all(smem_u32(&c->st_full[st][half]), round & 1u, wc, 0x93))
           goto done;
         ++sf_w;
         tc_fence_after_sync();
