@@ -287,6 +287,19 @@ __device__ __forceinline__ void mma_tk(uint32_t d_tmem, uint32_t a_tmem, uint32_
   }
 }
 
+// mma_tk over half of B's 128 rows (HALF 0: rows 0-63, HALF 1: 64-127), N = 64
+template <int DT, int D, int HALF>
+__device__ __forceinline__ void mma_tk_half(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
+                                            uint32_t idesc) {
+  using C = Cfg<DT, D>;
+  const uint64_t b0 = make_sdesc_sw128(sb + HALF * 64 * 128, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < C::kNumQKMma; ++k) {
+    const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
+    mma_ts<C::T::kKind>(d_tmem, a_tmem + k * 8, b0 + off, idesc, k > 0 ? 1u : 0u);
+  }
+}
+
 // D (+)= A B with A (128 x 128, 16-bit) in TMEM and B = a [128 rows x d]
 // tile (d contiguous) as the MN-major B operand
 template <int DT, int D>
@@ -369,8 +382,8 @@ struct DqCtrl {
   uint64_t qd_full, qd_empty;
   uint64_t k_full[NK], k_empty[NK];
   uint64_t v_full[NV], v_empty[NV];
-  uint64_t s_full;    // S(j), dP(j) in TMEM            (commit)
-  uint64_t sdp_free;  // elementwise read S(j), dP(j)    (8 warps)
+  uint64_t s_full[2];    // S(j), dP(j), keys 0-63 / 64-127, in TMEM (commit)
+  uint64_t sdp_free[2];  // elementwise read them (the 4 warps of that key half)
   uint64_t ds_full[2];  // dS(j), keys 0-63 / 64-127, in TMEM (4 warps each)
   uint64_t ds_free;   // dQ += dS(j) K_j done            (commit)
   uint64_t dq_full;   // last dQ MMA of the item done    (commit)
@@ -408,8 +421,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&c->v_full[s]), 1);
       mbar_init(smem_u32(&c->v_empty[s]), 1);
     }
-    mbar_init(smem_u32(&c->s_full), 1);
-    mbar_init(smem_u32(&c->sdp_free), 8);
+    mbar_init(smem_u32(&c->s_full[0]), 1);
+    mbar_init(smem_u32(&c->s_full[1]), 1);
+    mbar_init(smem_u32(&c->sdp_free[0]), 4);
+    mbar_init(smem_u32(&c->sdp_free[1]), 4);
     mbar_init(smem_u32(&c->ds_full[0]), 4);
     mbar_init(smem_u32(&c->ds_full[1]), 4);
     mbar_init(smem_u32(&c->ds_free), 1);
@@ -511,9 +526,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // and the tensor pipe runs this thread's operations in order), so
       // that S = Q K_j^T reads only K_j from shared memory
       copy_tile_to_tmem<DT, D>(tQ, sQ);
-      mma_tk<DT, D>(tS, tQ, sK + ks * C::kTileBytes, BC::kIdescSS);
-      mma_kk<DT, D>(tDP, sdO, sV + vs * C::kTileBytes, BC::kIdescSS);
-      mma_commit(smem_u32(&c->s_full));
+      // S and dP in two halves of the keys, each announced on its own, so
+      // that each elementwise warpgroup starts as soon as its half is there
+      // and frees it for the next block on its own
+      auto issue_sdp = [&](int h, int kslot, int vslot) {
+        const uint32_t sk = sK + kslot * C::kTileBytes, sv = sV + vslot * C::kTileBytes;
+        if (h == 0) {
+          mma_tk_half<DT, D, 0>(tS, tQ, sk, BC::kIdescSSHalf);
+          mma_kk_half<DT, D, 0>(tDP, sdO, sv, BC::kIdescSSHalf);
+        } else {
+          mma_tk_half<DT, D, 1>(tS + 64, tQ, sk, BC::kIdescSSHalf);
+          mma_kk_half<DT, D, 1>(tDP + 64, sdO, sv, BC::kIdescSSHalf);
+        }
+        mma_commit(smem_u32(&c->s_full[h]));
+      };
+      issue_sdp(0, ks, vs);
+      issue_sdp(1, ks, vs);
       mma_commit(smem_u32(&c->v_empty[vs]));
       if (w.n == 1) mma_commit(smem_u32(&c->qd_empty));
       for (int j = 0; j < w.n && ok; ++j) {
@@ -522,20 +550,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // S(j+1), dP(j+1) once the elementwise warps have read S(j), dP(j)
           next_slot(0, ks, kp);
           next_slot(1, vs, vp);
-          ok = wait_bar(smem_u32(&c->sdp_free), sf_w & 1u, wc, 0x53) &&
-               wait_bar(smem_u32(&c->k_full[ks]), kp, wc, 0x54) &&
-               wait_bar(smem_u32(&c->v_full[vs]), vp, wc, 0x54);
-          ++sf_w;
+          ok = wait_bar(smem_u32(&c->k_full[ks]), kp, wc, 0x54) &&
+               wait_bar(smem_u32(&c->v_full[vs]), vp, wc, 0x54) &&
+               wait_bar(smem_u32(&c->sdp_free[0]), sf_w & 1u, wc, 0x53);
           if (!ok) break;
           tc_fence_after_sync();
-          mma_tk<DT, D>(tS, tQ, sK + ks * C::kTileBytes, BC::kIdescSS);
-          mma_kk<DT, D>(tDP, sdO, sV + vs * C::kTileBytes, BC::kIdescSS);
-          mma_commit(smem_u32(&c->s_full));
+          issue_sdp(0, ks, vs);
+          if (!wait_bar(smem_u32(&c->sdp_free[1]), sf_w & 1u, wc, 0x53)) break;
+          ++sf_w;
+          tc_fence_after_sync();
+          issue_sdp(1, ks, vs);
           mma_commit(smem_u32(&c->v_empty[vs]));
           if (j + 2 == w.n) mma_commit(smem_u32(&c->qd_empty));
         } else {
           // keep the sdp_free phases in step: the last read of the item
-          ok = wait_bar(smem_u32(&c->sdp_free), sf_w & 1u, wc, 0x53);
+          ok = wait_bar(smem_u32(&c->sdp_free[0]), sf_w & 1u, wc, 0x53) &&
+               wait_bar(smem_u32(&c->sdp_free[1]), sf_w & 1u, wc, 0x53);
           ++sf_w;
           if (!ok) break;
         }
@@ -586,7 +616,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                                w.tile * kBlock + r];
       const float lse2 = lv.x, Dr = lv.y;
       for (int j = 0; j < w.n; ++j) {
-        if (!wait_bar_all(smem_u32(&c->s_full), sf_w & 1u, wc, 0x61)) goto done;
+        if (!wait_bar_all(smem_u32(&c->s_full[half]), sf_w & 1u, wc, 0x61)) goto done;
         ++sf_w;
         tc_fence_after_sync();
         // keys >= N masked; causal: keys after the query on the diagonal
@@ -609,7 +639,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&c->sdp_free));
+        if (lane == 0) mbar_arrive(smem_u32(&c->sdp_free[half]));
         // dS(j-1) must have been consumed before its columns are rewritten
         if (!first_ds) {
           if (!wait_bar_all(smem_u32(&c->ds_free), dsf_w & 1u, wc, 0x62)) goto done;
