@@ -839,6 +839,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!wait_bar(smem_u32(&c->st_full[st][1]), round & 1u, wc, 0x82)) break;
         tc_fence_after_sync();
         issue_sdp(1, sq);
+        // K and V serve only S^T and dP^T: free them for the next item's
+        // tiles once the item's last S^T and dP^T are issued
+        if (w.n == 1) mma_commit(smem_u32(&c->kv_empty));
       }
       for (int i = 0; i < w.n && ok; ++i) {
         const uint32_t sq = sSt + st * BC::kStageBytes;
@@ -876,9 +879,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!wait_bar(smem_u32(&c->st_full[st][1]), round & 1u, wc, 0x82)) break;
           tc_fence_after_sync();
           issue_sdp(1, sn);
+          if (i + 2 == w.n) mma_commit(smem_u32(&c->kv_empty));
         } else {
           mma_commit(smem_u32(&c->acc_full));
-          mma_commit(smem_u32(&c->kv_empty));
         }
       }
     }
