@@ -74,9 +74,12 @@ struct BwdCfg {
   // dK/dV kernel: K + V resident, ring of (Q_i, dO_i, vec_i)
   static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;
   static constexpr int kMiscDkv = 1024 + 512;
-  static constexpr int kStagesFit = (kSmemLimit - kMiscDkv - 2 * kTileBytes) / kStageBytes;
+  // the epilogue's per-warp staging: 8 elementwise warps x 32 rows x 64 bytes
+  static constexpr int kEpiBytes = 8 * 32 * 64;
+  static constexpr int kStagesFit =
+      (kSmemLimit - kMiscDkv - kEpiBytes - 2 * kTileBytes) / kStageBytes;
   static constexpr int kStages = kStagesFit > 4 ? 4 : kStagesFit;
-  static constexpr int kSmemDkv = kMiscDkv + 2 * kTileBytes + kStages * kStageBytes;
+  static constexpr int kSmemDkv = kMiscDkv + 2 * kTileBytes + kStages * kStageBytes + kEpiBytes;
   static_assert(kSlotsDq >= 2 && kStages >= 2, "backward shared-memory budget");
   static_assert(kSmemDq <= kSmemLimit && kSmemDkv <= kSmemLimit, "shared memory budget");
 
@@ -369,6 +372,38 @@ __device__ __forceinline__ void store_row_chunk(void* dst, const uint32_t (&v)[3
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i = 0; i < 4; ++i) d[i] = pack8_out<DT>(x + 8 * i);
+}
+
+// 32 fp32 values of each of a warp's 32 consecutive rows (lane l: row l),
+// times `f`, to the output type, through a 2 KiB shared-memory area of the
+// warp: written one row per lane, read back so that each global store
+// instruction covers 8 rows x 64 contiguous bytes (whole 32-byte sectors)
+// instead of 32 rows x 16 bytes.  Chunk c of row r sits at chunk
+// c ^ ((r >> 1) & 3) of its 64-byte row, which keeps both the row-per-lane
+// writes and the row-group reads free of bank conflicts.  out: this warp's
+// row 0 at the chunk's first column; pitch: bytes per row; n_valid: rows
+// that exist (the others are not stored).
+template <int DT>
+__device__ __forceinline__ void store_rows_staged(uint8_t* out, size_t pitch, int n_valid,
+                                                  const uint32_t (&v)[32], float f,
+                                                  uint32_t stage, uint32_t lane) {
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]) * f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    st_shared_v4(stage + lane * 64u + ((static_cast<uint32_t>(c) ^ ((lane >> 1) & 3u)) << 4),
+                 pack8_out<DT>(x + 8 * c));
+  __syncwarp();
+  const uint32_t ch = lane & 3u;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t rr = 8u * k + (lane >> 2);
+    const uint4 w = ld_shared_v4(stage + rr * 64u + ((ch ^ ((rr >> 1) & 3u)) << 4));
+    if (static_cast<int>(rr) < n_valid)
+      *reinterpret_cast<uint4*>(out + rr * pitch + ch * 16u) = w;
+  }
+  __syncwarp();  // the area is rewritten by the next call
 }
 
 // ---------------------------------------------------------------------------
@@ -713,7 +748,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sbase = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sK = smem_u32(sbase), sV = sK + C::kTileBytes, sSt = sV + C::kTileBytes;
   uint8_t* st_base = sbase + 2 * C::kTileBytes;
-  DkvCtrl<NST>* c = reinterpret_cast<DkvCtrl<NST>*>(sbase + 2 * C::kTileBytes + NST * BC::kStageBytes);
+  const uint32_t sEpi = sSt + NST * BC::kStageBytes;
+  DkvCtrl<NST>* c = reinterpret_cast<DkvCtrl<NST>*>(sbase + 2 * C::kTileBytes +
+                                                    NST * BC::kStageBytes + BC::kEpiBytes);
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
 
   if (threadIdx.x == 0) {
@@ -959,18 +996,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++af_w;
       tc_fence_after_sync();
       {
-        const int row = w.tile * kBlock + r;
+        // this warp's 32 rows, coalesced through its staging area
+        const int row0 = w.tile * kBlock + static_cast<int>(wq) * 32;
         const size_t off =
-            ((static_cast<size_t>(w.bh) * p.N + row) * D + (D / 2) * half) * C::T::kOutEsize;
+            ((static_cast<size_t>(w.bh) * p.N + row0) * D + (D / 2) * half) * C::T::kOutEsize;
         uint8_t* dv = static_cast<uint8_t*>(p.dv) + off;
         uint8_t* dk = static_cast<uint8_t*>(p.dk) + off;
+        const int n_valid = p.N - row0;
+        const size_t pitch = static_cast<size_t>(D) * C::T::kOutEsize;
+        const uint32_t stage = sEpi + (warp - 4u) * 2048u;
 #pragma unroll 1
         for (int cc = 0; cc < D / 2; cc += 32) {
           uint32_t v[32];
           tmem_ld_x32(tDV + cc, v);
-          if (row < p.N) store_row_chunk<DT>(dv + cc * C::T::kOutEsize, v, 1.0f);
+          store_rows_staged<DT>(dv + cc * C::T::kOutEsize, pitch, n_valid, v, 1.0f, stage, lane);
           tmem_ld_x32(tDK + cc, v);
-          if (row < p.N) store_row_chunk<DT>(dk + cc * C::T::kOutEsize, v, p.scale);
+          store_rows_staged<DT>(dk + cc * C::T::kOutEsize, pitch, n_valid, v, p.scale, stage, lane);
         }
       }
       tc_fence_before_sync();
