@@ -815,14 +815,33 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, uin
   uint32_t sc_waits[2] = {0, 0}, o_waits[2] = {0, 0};
   uint32_t iter = 0;
   bool ok = true;
+  // this item's first block of tile t was handled in the previous epilogue
+  bool first_done[2] = {false, false};
 
   for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < p.n_items; ++rnd) {
     const int it = round_item(rnd, p.n_items);
     if (it < 0) continue;
     const Item w = decode_item<NQT, CAUSAL>(it, p);
+    Item wn;
+    const bool has_next = next_item<NQT, CAUSAL>(rnd, p, wn);
+    // the next item's first block of tile t: its alpha (unused) consumed and
+    // O_t handed to its first P V, as soon as this item's O_t is read out
+    auto first_block_of_next = [&](int t) -> bool {
+      if (!wait_bar(smem_u32(&c->sc_full[t]), sc_waits[t] & 1u, wc, 0x31)) return false;
+      ++sc_waits[t];
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t][0]));
+      first_done[t] = true;
+      return true;
+    };
     for (int j = 0; j < w.nmax && ok; ++j) {
       for (int t = 0; t < NQT; ++t) {
         if (j >= w.n[t]) continue;
+        if (j == 0 && first_done[t]) {
+          first_done[t] = false;
+          continue;
+        }
         if (!wait_bar(smem_u32(&c->sc_full[t]), sc_waits[t] & 1u, wc, 0x31)) {
           ok = false;
           break;
@@ -891,6 +910,8 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, uin
 #pragma unroll
             for (int i = 0; i < 4; ++i) pk[4 * g + i] = pack8_out<DT>(x + 8 * i);
           }
+          // (no break on failure: every warp goes on through the named barriers)
+          if (has_next && bx == D / 64 - 1 && !first_block_of_next(t)) ok = false;
           if (issuer) {
             if constexpr (C::kStageBufs == 2)
               bulk_wait_read_1();
@@ -917,6 +938,7 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, uin
               st_shared_v4(stage_row + ((static_cast<uint32_t>(4 * g + i) ^ rsw) << 4),
                            pack8_out<DT>(x + 8 * i));
           }
+          if (has_next && bx == D / 64 - 1 && !first_block_of_next(t)) ok = false;
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
