@@ -70,14 +70,26 @@ __device__ __forceinline__ void unpack_chunk<__half>(const uint4 x, float (&v)[8
 // the caller (it is exact, and folds into the block scale).
 template <int E>
 __device__ __forceinline__ void wht16_lanes(float (&v)[E]) {
+  static_assert(E % 2 == 0, "pairs of channels per thread");
+  // stage h = 1 pairs neighbours: scalar adds and subtracts
 #pragma unroll
-  for (int h = 1; h < E; h <<= 1) {
+  for (int i = 0; i < E; i += 2) {
+    const float a = v[i], b = v[i + 1];
+    v[i] = __fadd_rn(a, b);
+    v[i + 1] = __fsub_rn(a, b);
+  }
+  // stages h = 2 .. E/2 pair (i, i + 1) with (i + h, i + h + 1): two channels
+  // per packed f32x2 add, and a - b as the packed fma b * (-1) + a, which
+  // rounds once exactly as the scalar subtraction
+  const uint64_t minus1 = f2_pack(-1.0f, -1.0f);
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
+  for (int h = 2; h < E; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
       if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = __fadd_rn(a, b);
-        v[i + h] = __fsub_rn(a, b);
+        const uint64_t a = f2_pack(v[i], v[i + 1]), b = f2_pack(v[i + h], v[i + h + 1]);
+        f2_unpack(f2_add(a, b), v[i], v[i + 1]);
+        f2_unpack(f2_fma(b, minus1, a), v[i + h], v[i + h + 1]);
       }
     }
   }
@@ -86,10 +98,12 @@ __device__ __forceinline__ void wht16_lanes(float (&v)[E]) {
   for (int h = E; h < 16; h <<= 1) {
     // other + v or other - v, rounded once: fma with a multiplier of +-1
     const float sgn = (lane & (h / E)) != 0 ? -1.0f : 1.0f;
+    const uint64_t sgn2 = f2_pack(sgn, sgn);
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
-      const float other = __shfl_xor_sync(0xffffffffu, v[i], h / E);
-      v[i] = __fmaf_rn(sgn, v[i], other);
+    for (int i = 0; i < E; i += 2) {
+      const float o0 = __shfl_xor_sync(0xffffffffu, v[i], h / E);
+      const float o1 = __shfl_xor_sync(0xffffffffu, v[i + 1], h / E);
+      f2_unpack(f2_fma(sgn2, f2_pack(v[i], v[i + 1]), f2_pack(o0, o1)), v[i], v[i + 1]);
     }
   }
 }
