@@ -47,8 +47,7 @@ struct CtrlTail {
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
-  uint32_t bcast;        // a value the epilogue's issuing thread shares
-  uint32_t bcast2[2];    // the pieces' flag counts, per tile
+  uint32_t bcast2[2];    // the pieces' flag counts, per tile (shared by the issuing thread)
   int rs[kMaxTailGrid + 1];  // tail_range_start of every CTA (and the end)
   float alpha[2][kBlock];
   // [segment parity][tile][row]: 1 / l of a whole tile, or l of a piece
