@@ -93,9 +93,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 /*
  * attn_fwd_workspace_size - bytes of device workspace attn_fwd_ws and
  * attn_fwd_fp8_ws need for head dim d and `dtype` on the current device
- * (it depends on the device's SM count, not on B, H or N); 0 for
- * ATTN_FP32, whose kernel takes no workspace, or for an invalid d, dtype
- * or device.
+ * (it depends on the device's SM count, not on B, H or N); 0 where the
+ * call never splits (ATTN_FP32, and d = 256, whose kernel runs whole items
+ * only) or for an invalid d, dtype or device.
  */
 unsigned long long attn_fwd_workspace_size(int d, int dtype);
 

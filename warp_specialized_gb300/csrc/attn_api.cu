@@ -117,6 +117,7 @@ int check_args(const void* q, const void* k, const void* v, const void* o, const
 // with num_sms SMs; 0 where no tail launch exists (exact fp32 path).
 unsigned long long fwd_workspace_size(int num_sms, int d, int dtype) {
   if (dtype != ATTN_FP16 && dtype != ATTN_BF16 && dtype != ATTN_FP8_E4M3) return 0ull;
+  if (d == 256) return 0ull;  // the d = 256 kernel runs whole items only
   return fwd_workspace_bytes(num_sms, d, fwd_nqt(d, dtype == ATTN_FP8_E4M3 ? 1 : 2));
 }
 
@@ -286,7 +287,7 @@ unsigned long long attn_fwd_workspace_size(int d, int dtype) {
 int attn_fwd_split_advised(int B, int H, int N, int d, int causal, int dtype) {
   if (B < 1 || H < 1 || N < 1 || (causal != 0 && causal != 1)) return 0;
   if (dtype != ATTN_FP16 && dtype != ATTN_BF16 && dtype != ATTN_FP8_E4M3) return 0;
-  if (d != 64 && d != 128 && d != 256) return 0;
+  if (d != 64 && d != 128) return 0;  // d = 256 runs whole items only
   const long long bh = static_cast<long long>(B) * H;
   if (bh > (1LL << 24) || N > (1 << 24) || bh * N > INT_MAX) return 0;
   int dev = -1;

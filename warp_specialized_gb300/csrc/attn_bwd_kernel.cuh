@@ -261,34 +261,6 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t sa, uint32_t sb
   }
 }
 
-// A 128-row, K-major tile (Q) from shared memory into Tensor Memory, in the
-// layout a tcgen05.mma A operand takes there: row r in lane r, elements
-// (2m, 2m + 1) in column m.  One 32-byte K slice per copy, the slices
-// exactly those an SS MMA would read for each K step.
-template <int DT, int D>
-__device__ __forceinline__ void copy_tile_to_tmem(uint32_t t, uint32_t s) {
-  using C = Cfg<DT, D>;
-  const uint64_t a0 = make_sdesc_sw128(s, 16, 1024);
-#pragma unroll
-  for (int k = 0; k < C::kNumQKMma; ++k) {
-    const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
-    tmem_cp_128x256b(t + k * 8, a0 + off);
-  }
-}
-
-// A x B^T with A (128 rows, K-major) in Tensor Memory and B K-major in
-// shared memory (S = Q K^T with Q copied into TMEM)
-template <int DT, int D>
-__device__ __forceinline__ void mma_tk(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
-                                       uint32_t idesc) {
-  using C = Cfg<DT, D>;
-  const uint64_t b0 = make_sdesc_sw128(sb, 16, 1024);
-#pragma unroll
-  for (int k = 0; k < C::kNumQKMma; ++k) {
-    const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
-    mma_ts<C::T::kKind>(d_tmem, a_tmem + k * 8, b0 + off, idesc, k > 0 ? 1u : 0u);
-  }
-}
 
 // mma_tk over half of B's 128 rows (HALF 0: rows 0-63, HALF 1: 64-127), N = 64
 template <int DT, int D, int HALF>

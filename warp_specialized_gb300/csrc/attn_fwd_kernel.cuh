@@ -98,8 +98,15 @@ struct Cfg {
   // two query tiles per CTA when both S and O of both fit in Tensor Memory
   // (2 * (128 + D) <= 512 columns) and in shared memory
   static constexpr int kNQT = (D <= 128 && kTileBytes <= 32768) ? 2 : 1;
+  // d = 256 (one query tile per CTA): Q is copied into Tensor Memory once per
+  // item (tcgen05.cp) and taken from there as the A operand of S = Q K^T,
+  // and the Q tile's shared memory joins the K/V ring, which then holds
+  // three 64 KiB tiles instead of two, so that K_{j+1} loads while K_j and
+  // V_j are in use.  (TMEM: S 128 + O 256 + Q 128 = 512 columns.)
+  static constexpr bool kQTmem = D == 256;
+  static constexpr int kQBufTiles = kQTmem ? 0 : kNQT;  // Q tiles in shared memory
   // issue the next work item's first S behind this item's last P V
-  static constexpr bool kEarlyS0 = true;
+  static constexpr bool kEarlyS0 = !kQTmem;
   // epilogue: read and pack a whole 64-column box of O before waiting for
   // the staging box (measured +3% with e4m3; at 16 bits the extra live
   // registers spill and it loses up to 1%)
@@ -114,7 +121,7 @@ struct Cfg {
   static constexpr int kStageBufs = DT == 3 ? 2 : 1;
   static constexpr int kStageTotal = kStageBufs * kStageBytes;
   static constexpr int kSlotsFit =
-      (kSmemLimit - kMiscBytes - kStageTotal - kNQT * kTileBytes) / kTileBytes;
+      (kSmemLimit - kMiscBytes - kStageTotal - kQBufTiles * kTileBytes) / kTileBytes;
   static constexpr int kSlots = kSlotsFit > kMaxSlots ? kMaxSlots : kSlotsFit;
   static_assert(kSlots >= 2, "the K/V ring needs at least two slots");
   // Ring stages.  With four or more slots a stage is a pair of slots that
@@ -126,7 +133,7 @@ struct Cfg {
   static constexpr int kStages = kPair ? kSlots / 2 : kSlots;
   static __host__ __device__ constexpr int v_slot(int st) { return kPair ? 2 * st : st; }
   static __host__ __device__ constexpr int k_slot(int st) { return kPair ? 2 * st + 1 : st; }
-  static constexpr int kSmemBytes = kMiscBytes + (kNQT + kSlots) * kTileBytes + kStageTotal;
+  static constexpr int kSmemBytes = kMiscBytes + (kQBufTiles + kSlots) * kTileBytes + kStageTotal;
   // a piece's (O, m, l) in the tail launch's workspace: O as [D / 4][128]
   // float4 (four columns of one row per 16 bytes, the 128 rows of a column
   // quad contiguous, so that a warp's 16-byte accesses are contiguous),
@@ -148,6 +155,9 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static __host__ __device__ constexpr uint32_t s_col(int t) { return t * kBlock; }
   static __host__ __device__ constexpr uint32_t o_col(int t) { return kNQT * kBlock + t * D; }
+  // Q in Tensor Memory (kQTmem): 16-bit pairs, D / 2 columns
+  static __host__ __device__ constexpr uint32_t q_col() { return kNQT * (kBlock + D); }
+  static_assert(!kQTmem || (kNQT == 1 && q_col() + D / 2 <= 512), "Tensor Memory budget (Q)");
   static_assert(kNQT * (kBlock + D) <= 512, "Tensor Memory budget");
 };
 
@@ -307,7 +317,7 @@ __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   using C = Cfg<DT, D>;
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
   const uint8_t* sq = sbase;
-  const uint32_t skv = smem_u32(sbase + C::kNQT * C::kTileBytes);
+  const uint32_t skv = smem_u32(sbase + C::kQBufTiles * C::kTileBytes);
   uint32_t q_uses[2] = {0, 0};
   RingPos ring;
   uint32_t stages = 0;  // ring stages filled
@@ -345,8 +355,22 @@ __device__ void role_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
     const Item w = decode_item<C::kNQT, CAUSAL>(it, p);
     Item wn;
     const bool has_next = next_item<C::kNQT, CAUSAL>(rnd, p, wn);
+    if constexpr (C::kQTmem) {
+      // the item's Q tile through the ring, ahead of its first K
+      int st;
+      uint32_t par;
+      ring.next<C::kStages>(st, par);
+      if (!wait_bar(smem_u32(&c->kv_empty[st]), par ^ 1u, wc, 0x02)) break;
+      const uint32_t full = smem_u32(&c->kv_full[st]);
+      mbar_arrive_expect_tx(full, C::kTileBytes);
+      const uint32_t dst = skv + C::k_slot(st) * C::kTileBytes;
 #pragma unroll
-    for (int t = 0; t < C::kNQT; ++t) {
+      for (int b = 0; b < C::kNumBox; ++b)
+        tma_load_3d(dst + b * C::kBoxBytes, tmQ, b * C::kBoxInner, w.qt0 * kBlock, w.bh, full);
+      ++stages;
+    }
+#pragma unroll
+    for (int t = 0; t < (C::kQTmem ? 0 : C::kNQT); ++t) {
       const uint32_t full = smem_u32(&c->q_full[t]);
       if (!wait_bar(smem_u32(&c->q_empty[t]), (q_uses[t] & 1u) ^ 1u, wc, 0x01)) {
         ok = false;
@@ -407,6 +431,35 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
   return (d & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(d) + off16);
 }
 
+// A 128-row, K-major tile (Q) from shared memory into Tensor Memory, in the
+// layout a tcgen05.mma A operand takes there: row r in lane r, elements
+// (2m, 2m + 1) in column m.  One 32-byte K slice per copy, the slices
+// exactly those an SS MMA would read for each K step.
+template <int DT, int D>
+__device__ __forceinline__ void copy_tile_to_tmem(uint32_t t, uint32_t s) {
+  using C = Cfg<DT, D>;
+  const uint64_t a0 = make_sdesc_sw128(s, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < C::kNumQKMma; ++k) {
+    const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
+    tmem_cp_128x256b(t + k * 8, a0 + off);
+  }
+}
+
+// A x B^T with A (128 rows, K-major) in Tensor Memory and B K-major in
+// shared memory (S = Q K^T with Q copied into TMEM)
+template <int DT, int D>
+__device__ __forceinline__ void mma_tk(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
+                                       uint32_t idesc) {
+  using C = Cfg<DT, D>;
+  const uint64_t b0 = make_sdesc_sw128(sb, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < C::kNumQKMma; ++k) {
+    const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
+    mma_ts<C::T::kKind>(d_tmem, a_tmem + k * 8, b0 + off, idesc, k > 0 ? 1u : 0u);
+  }
+}
+
 template <int DT, int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk) {
   using C = Cfg<DT, D>;
@@ -446,20 +499,29 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
   constexpr int NQT = C::kNQT;
   const WaitCtx wc{&c->abort, p.timeout_ns, p.status, p.where};
   const uint32_t sq = smem_u32(sbase);
-  const uint32_t skv = sq + NQT * C::kTileBytes;
+  const uint32_t skv = sq + C::kQBufTiles * C::kTileBytes;
   uint32_t q_waits[2] = {0, 0}, p_waits[2] = {0, 0};
   RingPos ring;
   bool ok = true;
 
+  // S_t = Q_t K^T with K in shared memory at sk: Q_t from shared memory, or
+  // (kQTmem) from Tensor Memory
+  auto issue_s = [&](int t, uint32_t sk) {
+    if constexpr (C::kQTmem)
+      mma_tk<DT, D>(tbase + C::s_col(t), tbase + C::q_col(), sk, C::kIdescQK);
+    else
+      issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes, sk);
+  };
   // S_t(0) of item w with K_0 in stage ks; false when a wait gave up
   auto issue_s0 = [&](const Item& w, int t, int ks) -> bool {
-    if (!wait_bar(smem_u32(&c->q_full[t]), q_waits[t] & 1u, wc, 0x12)) return false;
-    ++q_waits[t];
-    tc_fence_after_sync();
-    issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes,
-                    skv + C::k_slot(ks) * C::kTileBytes);
+    if constexpr (!C::kQTmem) {
+      if (!wait_bar(smem_u32(&c->q_full[t]), q_waits[t] & 1u, wc, 0x12)) return false;
+      ++q_waits[t];
+      tc_fence_after_sync();
+    }
+    issue_s(t, skv + C::k_slot(ks) * C::kTileBytes);
     mma_commit(smem_u32(&c->s_full[t]));
-    if (w.n[t] == 1) mma_commit(smem_u32(&c->q_empty[t]));
+    if (!C::kQTmem && w.n[t] == 1) mma_commit(smem_u32(&c->q_empty[t]));
     return true;
   };
 
@@ -478,6 +540,18 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
     const int walk = w.nmax;
     Item wn;
     const bool has_next = next_item<NQT, CAUSAL>(rnd, p, wn);
+    if constexpr (C::kQTmem) {
+      // the item's Q from its ring stage into Tensor Memory (after the
+      // previous item's last S, which read the old Q: this thread's tensor
+      // operations run in order), then the stage back to the producer
+      int qs;
+      uint32_t qpar;
+      ring.next<C::kStages>(qs, qpar);
+      if (!wait_bar(smem_u32(&c->kv_full[qs]), qpar, wc, 0x12)) break;
+      tc_fence_after_sync();
+      copy_tile_to_tmem<DT, D>(tbase + C::q_col(), skv + C::k_slot(qs) * C::kTileBytes);
+      mma_commit(smem_u32(&c->kv_empty[qs]));
+    }
     if (!s0_issued) {
       // S_t(0) for every tile
       int ks = held;
@@ -541,9 +615,9 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
             }
             k_ready = true;
           }
-          issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes, sk);
+          issue_s(t, sk);
           mma_commit(smem_u32(&c->s_full[t]));
-          if (j + 2 == w.n[t]) mma_commit(smem_u32(&c->q_empty[t]));
+          if (!C::kQTmem && j + 2 == w.n[t]) mma_commit(smem_u32(&c->q_empty[t]));
         }
         if constexpr (kEarly) {
           // only where K_0 and Q_t are already here: the other tile's P V
@@ -969,8 +1043,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // tiles need 1024-byte alignment (128-byte swizzle atoms)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* sbase = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  const uint32_t stage = smem_u32(sbase + (C::kNQT + C::kSlots) * C::kTileBytes);
-  CtrlT* c = reinterpret_cast<CtrlT*>(sbase + (C::kNQT + C::kSlots) * C::kTileBytes +
+  const uint32_t stage = smem_u32(sbase + (C::kQBufTiles + C::kSlots) * C::kTileBytes);
+  CtrlT* c = reinterpret_cast<CtrlT*>(sbase + (C::kQBufTiles + C::kSlots) * C::kTileBytes +
                                       C::kStageTotal);
 
   const uint32_t warp = threadIdx.x >> 5;

@@ -89,7 +89,6 @@ template <int DT, int D, bool CAUSAL>
 int launch_instance(const LaunchArgs& a) {
   using C = Cfg<DT, D>;
   auto kern = attn_fwd_kernel<DT, D, CAUSAL>;
-  auto tail_kern = attn_fwd_tail_kernel<DT, D, CAUSAL>;
   static std::atomic<int> ready[kMaxDevices], ready_tail[kMaxDevices];
   if (a.device < 0 || a.device >= kMaxDevices) return kErrDevice;
   int rc = prepare_fwd_kernel(kern, C::kSmemBytes, a.device, ready);
@@ -125,15 +124,19 @@ int launch_instance(const LaunchArgs& a) {
 
   // With a workspace, the main kernel runs whole rounds of num_sms items
   // and the tail launch the rest; without one, one launch runs all items.
-  const int n_all = p.n_items;
+  // (d = 256 keeps its Q in Tensor Memory, a layout the tail kernel does not
+  // have: it always runs whole items.)
   const TailPlan plan =
-      a.workspace ? plan_tail(p.BH, p.n_pairs, p.nkv, C::kNQT, CAUSAL, a.num_sms,
-                              tail_max_pieces(D, C::kEsize))
-                  : TailPlan{};
+      (a.workspace && !C::kQTmem)
+          ? plan_tail(p.BH, p.n_pairs, p.nkv, C::kNQT, CAUSAL, a.num_sms,
+                      tail_max_pieces(D, C::kEsize))
+          : TailPlan{};
   const int tail = plan.items;
   const int tail_grid = plan.grid;
+  if constexpr (!C::kQTmem) {
   if (tail > 0) {
-    rc = prepare_fwd_kernel(tail_kern, TailCfg<DT, D>::kSmemBytes, a.device, ready_tail);
+    rc = prepare_fwd_kernel(attn_fwd_tail_kernel<DT, D, CAUSAL>, TailCfg<DT, D>::kSmemBytes,
+                            a.device, ready_tail);
     if (rc != kOk) return rc;
     if (a.workspace_bytes < fwd_workspace_bytes(a.num_sms, D, C::kNQT)) return kErrInvalidArg;
     p.tail_start = plan.start;
@@ -152,6 +155,7 @@ int launch_instance(const LaunchArgs& a) {
       return kErrCuda;
     }
   }
+  }
   // persistent grid: one CTA per SM (the shared-memory budget allows no
   // second), never more CTAs than work items
   if (p.n_items > 0) {
@@ -166,6 +170,7 @@ int launch_instance(const LaunchArgs& a) {
       return kErrCuda;
     }
   }
+  if constexpr (!C::kQTmem) {
   if (tail > 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tail_grid, 1, 1);
@@ -182,11 +187,14 @@ int launch_instance(const LaunchArgs& a) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
     }
-    if (cudaLaunchKernelEx(&cfg, tail_kern, mq, mk, mv, mo, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, attn_fwd_tail_kernel<DT, D, CAUSAL>, mq, mk, mv, mo, p) !=
+        cudaSuccess) {
       cudaGetLastError();
       return kErrCuda;
     }
   }
+  }
+  (void)tail_grid;
   return kOk;
 }
 
