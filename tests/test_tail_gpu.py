@@ -108,7 +108,6 @@ SPLIT_SMALL = [
     (1, 1, 2048, 128, "bf16"),   # 8 items, no main launch, 16 CTAs of 8 blocks
     (1, 2, 1500, 128, "bf16"),   # ragged: 12 items of 12 blocks, pieces 8 + 4
     (1, 3, 1500, 64, "bf16"),    # d = 64
-    (1, 2, 1500, 256, "bf16"),   # d = 256: one query tile per item
     (1, 2, 1500, 128, "fp16"),
     (1, 2, 1500, 128, "fp8"),
     (1, 1, 8192, 128, "bf16"),   # 32 items of 64 blocks over 152 CTAs: ~5 pieces each
@@ -121,6 +120,20 @@ SPLIT_SMALL = [
 @pytest.mark.parametrize("B,H,N,d,dtype", SPLIT_SMALL, ids=lambda x: str(x))
 def test_split_items_small(B, H, N, d, dtype, causal):
     _check_split(B, H, N, d, dtype, causal, seed=500 + N + d + H)
+
+
+def test_d256_runs_whole_items():
+    """d = 256 keeps Q in Tensor Memory and its shared-memory tile in the
+    K/V ring, which leaves no room for a piece merge: it takes no workspace,
+    is never advised a split, and a requested split runs whole items."""
+    import warp_specialized_gb300 as ws
+    assert ws.attn_fwd_workspace_size(256, ws.ATTN_BF16) == 0
+    assert ws.attn_fwd_workspace_size(256, ws.ATTN_FP8_E4M3) == 0
+    assert not ws.attn_fwd_split_advised(1, 1, 8192, 256, False, ws.ATTN_BF16)
+    for causal in (False, True):
+        inp = ai.make_inputs(1, 2, 1500, 256, "bf16", seed=1756 + causal)
+        o, lse = run_gpu(inp, causal, split_tail=True)
+        compare(inp, causal, o, lse)
 
 
 def test_split_cuts_items():
