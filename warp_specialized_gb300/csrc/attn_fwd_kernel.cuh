@@ -151,14 +151,27 @@ struct Cfg {
   static constexpr uint32_t kIdescQK = make_idesc(T::kFmt, T::kFmt, false, kBlock, kBlock);
   static constexpr uint32_t kIdescPV = make_idesc(T::kFmt, T::kFmt, true, D, kBlock);
 
+  // S lookahead (two query tiles with D <= 64): a third S buffer fits in
+  // Tensor Memory (3 x 128 + 2 x D <= 512 columns), so the S buffers are
+  // used in turn, in the order the S products are issued, and a tile's
+  // S(j + 1) goes out before its P(j) V instead of after it: the softmax
+  // then moves on to block j + 1 without waiting for P(j) V and S(j + 1) to
+  // pass through the tensor pipe.  Barriers that could otherwise complete
+  // a second phase before their waiter has seen the first (s_full, the
+  // second half of p_full) are kept in two sets used in turn.
+  static constexpr bool kSLook = kNQT == 2 && 3 * kBlock + 2 * D <= 512;
+  static constexpr int kSBufs = kSLook ? 3 : kNQT;
+  static constexpr int kBarSets = kSLook ? 2 : 1;
+
   // Tensor Memory columns
   static constexpr uint32_t kTmemCols = 512;
   static __host__ __device__ constexpr uint32_t s_col(int t) { return t * kBlock; }
-  static __host__ __device__ constexpr uint32_t o_col(int t) { return kNQT * kBlock + t * D; }
+  static __host__ __device__ constexpr uint32_t s_buf_col(uint32_t b) { return b * kBlock; }
+  static __host__ __device__ constexpr uint32_t o_col(int t) { return kSBufs * kBlock + t * D; }
   // Q in Tensor Memory (kQTmem): 16-bit pairs, D / 2 columns
   static __host__ __device__ constexpr uint32_t q_col() { return kNQT * (kBlock + D); }
   static_assert(!kQTmem || (kNQT == 1 && q_col() + D / 2 <= 512), "Tensor Memory budget (Q)");
-  static_assert(kNQT * (kBlock + D) <= 512, "Tensor Memory budget");
+  static_assert(kSBufs * kBlock + kNQT * D <= 512, "Tensor Memory budget");
 };
 
 struct AttnParams {
@@ -268,18 +281,29 @@ template <int NSLOT>
 struct Ctrl {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[NSLOT], kv_empty[NSLOT];
-  uint64_t s_full[2];    // S_t(j) in TMEM            (MMA commit)
-  // P_t(j) keys 0-63 in TMEM and O_t rescaled for block j (4 softmax + 4
-  // correction warps); P_t(j) keys 64-127 in TMEM (4 softmax warps)
-  uint64_t p_full[2][2];
+  uint64_t s_full[2][2];  // S_t(j) in TMEM, [tile][set]  (MMA commit)
+  // [t][0]: P_t(j) keys 0-63 in TMEM and O_t rescaled for block j (4
+  // softmax + 4 correction warps); [t][1 + set]: P_t(j) keys 64-127 in
+  // TMEM (4 softmax warps)
+  uint64_t p_full[2][3];
   uint64_t sc_full[2];   // alpha_t(j) in smem        (4 softmax warps)
   uint64_t o_full[2];    // P_t V of the item's last block done (MMA commit)
+  uint64_t pv_done[2];   // S lookahead: P_t V of a block that is not the last (MMA commit)
   uint64_t drain;        // all MMAs done             (MMA commit)
   uint32_t tmem_base;
   uint32_t abort;        // set when a wait in this CTA ran out
   float alpha[2][kBlock];
   float inv_l[2][2][kBlock];  // [item parity][tile][row]
 };
+
+// The k-th use (from 0) of a barrier kept in `sets` copies used in turn:
+// which copy, and the parity of its phase.
+__device__ __forceinline__ uint32_t bar_set(uint32_t k, int sets) {
+  return sets == 2 ? (k & 1u) : 0u;
+}
+__device__ __forceinline__ uint32_t bar_par(uint32_t k, int sets) {
+  return sets == 2 ? ((k >> 1) & 1u) : (k & 1u);
+}
 
 // Bounded wait: true when the phase with `parity` has completed; false when
 // another thread of this CTA gave up or the limit ran out (then the status
@@ -501,16 +525,33 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
   const uint32_t sq = smem_u32(sbase);
   const uint32_t skv = sq + C::kQBufTiles * C::kTileBytes;
   uint32_t q_waits[2] = {0, 0}, p_waits[2] = {0, 0};
+  uint32_t s_cnt[2] = {0, 0};  // S products issued per tile
+  uint32_t s_next = 0;         // S lookahead: the buffer the next S goes to
+  // S buffer of each tile's S products not yet consumed by P V (at most
+  // two a tile): two bits at bit 4 * t + 2 * (count & 1)
+  uint32_t pbuf = 0x50u;
   RingPos ring;
   bool ok = true;
 
-  // S_t = Q_t K^T with K in shared memory at sk: Q_t from shared memory, or
-  // (kQTmem) from Tensor Memory
+  // S_t = Q_t K^T with K in shared memory at sk, committed to s_full: Q_t
+  // from shared memory, or (kQTmem) from Tensor Memory; into the tile's own
+  // S buffer, or (S lookahead) the next one in turn
   auto issue_s = [&](int t, uint32_t sk) {
+    const uint32_t b = C::kSLook ? s_next : static_cast<uint32_t>(t);
+    const uint32_t d_tmem = tbase + C::s_buf_col(b);
     if constexpr (C::kQTmem)
-      mma_tk<DT, D>(tbase + C::s_col(t), tbase + C::q_col(), sk, C::kIdescQK);
+      mma_tk<DT, D>(d_tmem, tbase + C::q_col(), sk, C::kIdescQK);
     else
-      issue_qk<DT, D>(tbase + C::s_col(t), sq + t * C::kTileBytes, sk);
+      issue_qk<DT, D>(d_tmem, sq + t * C::kTileBytes, sk);
+    if constexpr (C::kSLook) {
+      const uint32_t sh = 4u * static_cast<uint32_t>(t) + 2u * (s_cnt[t] & 1u);
+      pbuf = (pbuf & ~(3u << sh)) | (b << sh);
+      mma_commit(smem_u32(&c->s_full[t][bar_set(s_cnt[t], C::kBarSets)]));
+      ++s_cnt[t];
+      s_next = s_next == 2u ? 0u : s_next + 1u;
+    } else {
+      mma_commit(smem_u32(&c->s_full[t][0]));
+    }
   };
   // S_t(0) of item w with K_0 in stage ks; false when a wait gave up
   auto issue_s0 = [&](const Item& w, int t, int ks) -> bool {
@@ -520,7 +561,6 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
       tc_fence_after_sync();
     }
     issue_s(t, skv + C::k_slot(ks) * C::kTileBytes);
-    mma_commit(smem_u32(&c->s_full[t]));
     if (!C::kQTmem && w.n[t] == 1) mma_commit(smem_u32(&c->q_empty[t]));
     return true;
   };
@@ -583,46 +623,65 @@ __device__ void role_mma(uint8_t* sbase, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t t
       const uint32_t sv = skv + C::v_slot(vs) * C::kTileBytes;
       const uint32_t sk = skv + C::k_slot(ns) * C::kTileBytes;
       for (int t = 0; t < NQT && ok; ++t) {
+        // S_t(j + 1): behind P_t(j) V, or (S lookahead) ahead of it
+        auto next_s = [&]() -> bool {
+          if (j + 1 < w.n[t]) {
+            if (!k_ready) {
+              if (!wait_bar(smem_u32(&c->kv_full[ns]), npar, wc, 0x16)) return false;
+              k_ready = true;
+            }
+            issue_s(t, sk);
+            if (!C::kQTmem && j + 2 == w.n[t]) mma_commit(smem_u32(&c->q_empty[t]));
+          }
+          return true;
+        };
+        if (C::kSLook && !next_s()) {
+          ok = false;
+          break;
+        }
         if (j < w.n[t]) {
           // first key half as soon as its P and the rescaled O are there
           // (p_full[t][0] counts the softmax and the correction warps),
           // overlapping the softmax of the second half
-          if (!wait_bar(smem_u32(&c->p_full[t][0]), p_waits[t] & 1u, wc, 0x14)) {
+          const uint32_t pk = p_waits[t];
+          if (!wait_bar(smem_u32(&c->p_full[t][0]), pk & 1u, wc, 0x14)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          issue_pv_half<DT, D, 0>(tbase + C::o_col(t), tbase + C::s_col(t), sv, j > 0);
-          if (!wait_bar(smem_u32(&c->p_full[t][1]), p_waits[t] & 1u, wc, 0x18)) {
+          const uint32_t p_tmem =
+              C::kSLook ? tbase + C::s_buf_col((pbuf >> (4u * static_cast<uint32_t>(t) + 2u * (pk & 1u))) & 3u)
+                        : tbase + C::s_col(t);
+          issue_pv_half<DT, D, 0>(tbase + C::o_col(t), p_tmem, sv, j > 0);
+          if (!wait_bar(smem_u32(&c->p_full[t][1 + bar_set(pk, C::kBarSets)]),
+                        bar_par(pk, C::kBarSets), wc, 0x18)) {
             ok = false;
             break;
           }
           ++p_waits[t];
           tc_fence_after_sync();
-          issue_pv_half<DT, D, 1>(tbase + C::o_col(t), tbase + C::s_col(t), sv, true);
-          // O_t is complete for the epilogue after the tile's last block;
-          // for earlier blocks the correction warps need no signal of their
-          // own: they rescale O_t for block j + 1 only after alpha_t(j + 1),
-          // which the softmax publishes after S_t(j + 1) completed, and that
-          // commit tracks this P_t V too
-          if (j + 1 == w.n[t]) mma_commit(smem_u32(&c->o_full[t]));
+          issue_pv_half<DT, D, 1>(tbase + C::o_col(t), p_tmem, sv, true);
+          // O_t is complete for the epilogue after the tile's last block.
+          // For earlier blocks the correction warps rescale O_t for block
+          // j + 1 only once this product is done: they wait for pv_done
+          // (S lookahead), or else for alpha_t(j + 1), which the softmax
+          // publishes after S_t(j + 1) completed, and that commit, issued
+          // behind this product, tracks it too.
+          if (j + 1 == w.n[t])
+            mma_commit(smem_u32(&c->o_full[t]));
+          else if constexpr (C::kSLook)
+            mma_commit(smem_u32(&c->pv_done[t]));
         }
-        if (j + 1 < w.n[t]) {
-          if (!k_ready) {
-            if (!wait_bar(smem_u32(&c->kv_full[ns]), npar, wc, 0x16)) {
-              ok = false;
-              break;
-            }
-            k_ready = true;
-          }
-          issue_s(t, sk);
-          mma_commit(smem_u32(&c->s_full[t]));
-          if (!C::kQTmem && j + 2 == w.n[t]) mma_commit(smem_u32(&c->q_empty[t]));
+        if (!C::kSLook && !next_s()) {
+          ok = false;
+          break;
         }
         if constexpr (kEarly) {
           // only where K_0 and Q_t are already here: the other tile's P V
           // must not wait behind them
-          if (ahead) {
+          // (S lookahead: S products go out in tile order, which the
+          // softmax's choice of buffer assumes)
+          if (ahead && (!C::kSLook || t == 0 || s0_done[0])) {
             if (!k_ready) k_ready = mbar_test_wait(smem_u32(&c->kv_full[ns]), npar);
             if (k_ready && mbar_test_wait(smem_u32(&c->q_full[t]), q_waits[t] & 1u)) {
               ok = issue_s0(wn, t, ns);
@@ -769,6 +828,10 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
   const float sl2 = p.scale_log2;
   uint32_t s_waits = 0;
   uint32_t iter = 0;
+  // S lookahead: S products fill the three buffers in turn, in issue order
+  // (blocks in order, tile 0 before tile 1 within a block); seq3 is the
+  // number of S products of the earlier items, mod 3
+  [[maybe_unused]] uint32_t seq3 = 0;
 
   for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < p.n_items; ++rnd) {
     const int it = round_item(rnd, p.n_items);
@@ -787,8 +850,18 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
     }
     float* const inv_l_dst = &c->inv_l[iter & 1u][t][r];
     float* const alpha_dst = &c->alpha[t][r];
+    // S lookahead: this tile's S buffer for block 0 (both tiles have one:
+    // n[0] >= 1)
+    [[maybe_unused]] uint32_t sb = (seq3 + static_cast<uint32_t>(t)) % 3u;
     for (int j = 0; j < n; ++j) {
-      if (!wait_bar(smem_u32(&c->s_full[t]), s_waits & 1u, wc, 0x21)) return;
+      // S lookahead: s_full in two sets used in turn, S in buffer sb
+      uint32_t sa = taddr;
+      if constexpr (C::kSLook) {
+        if (!wait_bar(smem_u32(&c->s_full[t][s_waits & 1u]), (s_waits >> 1) & 1u, wc, 0x21)) return;
+        sa = taddr - C::s_col(t) + C::s_buf_col(sb);
+      } else {
+        if (!wait_bar(smem_u32(&c->s_full[t][0]), s_waits & 1u, wc, 0x21)) return;
+      }
       ++s_waits;
       tc_fence_after_sync();
       // mask: keys >= N in the last block; keys after the query on the
@@ -801,7 +874,7 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
       float s[kBlock];
       {
         uint32_t raw[kBlock];
-        tmem_ld_2x64(taddr, raw);
+        tmem_ld_2x64(sa, raw);
 #pragma unroll
         for (int i = 0; i < kBlock; ++i) s[i] = __uint_as_float(raw[i]);
       }
@@ -825,6 +898,13 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
       }
       // subtraction reference: 0 while every key so far is masked
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      if constexpr (C::kSLook) {
+        // the correction warps have read alpha of the previous block (and
+        // so waited for its P V): without the round trip through the tensor
+        // pipe between two blocks nothing else orders this store after
+        // their read, nor keeps p_full from running two phases ahead
+        if (s_waits > 1u && !wait_bar(smem_u32(&c->p_full[t][0]), s_waits & 1u, wc, 0x22)) return;
+      }
       *alpha_dst = alpha;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c->sc_full[t]));
@@ -833,20 +913,26 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
       // halves of 64 keys: the first is handed to the MMA issuer while the
       // second is computed
       const float neg_m = -m_use;
-      const float sum0 = exp_store_chunk<DT, 0, 64>(s, sl2j, neg_m, taddr);
+      const float sum0 = exp_store_chunk<DT, 0, 64>(s, sl2j, neg_m, sa);
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t][0]));
-      const float sum1 = exp_store_chunk<DT, 64, 64>(s, sl2j, neg_m, taddr + C::kPCols / 2);
+      const float sum1 = exp_store_chunk<DT, 64, 64>(s, sl2j, neg_m, sa + C::kPCols / 2);
       l_run = alpha * l_run + (sum0 + sum1);
       tmem_st_wait();
       // hand 1/l to the epilogue before the last P is announced
       if (j == n - 1) *inv_l_dst = __frcp_rn(l_run);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t][1]));
+      if constexpr (C::kSLook) {
+        if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t][1 + ((s_waits - 1u) & 1u)]));
+        sb = (sb + (t == 0 ? 2u : (j + 1 < w.n[0] ? 2u : 1u))) % 3u;
+      } else {
+        if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t][1]));
+      }
     }
+    if constexpr (C::kSLook) seq3 = (seq3 + static_cast<uint32_t>(w.n[0] + w.n[1])) % 3u;
     // LSE (natural log) of the real rows
     const int row = qt * kBlock + r;
     if (row < p.N) {
@@ -886,7 +972,7 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, uin
   const bool issuer = r == 0;  // issues and tracks the TMA stores
   const uint32_t stage_row0 = stage + static_cast<uint32_t>(r) * 128u;
   uint32_t nbox = 0;  // boxes stored (selects the staging buffer)
-  uint32_t sc_waits[2] = {0, 0}, o_waits[2] = {0, 0};
+  uint32_t sc_waits[2] = {0, 0}, o_waits[2] = {0, 0}, pv_waits[2] = {0, 0};
   uint32_t iter = 0;
   bool ok = true;
   // this item's first block of tile t was handled in the previous epilogue
@@ -923,8 +1009,16 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, uin
         ++sc_waits[t];
         const float alpha = c->alpha[t][r];
         if (j > 0) {
-          // P_t V_{j-1} has completed: alpha_t(j) was published after
-          // S_t(j), whose commit came after that product
+          // P_t V_{j-1} has completed: under S lookahead its own commit
+          // says so; otherwise alpha_t(j) was published after S_t(j), whose
+          // commit came after that product
+          if constexpr (C::kSLook) {
+            if (!wait_bar(smem_u32(&c->pv_done[t]), pv_waits[t] & 1u, wc, 0x34)) {
+              ok = false;
+              break;
+            }
+            ++pv_waits[t];
+          }
           tc_fence_after_sync();
           // exact skip: a warp whose 32 rows all kept their max has alpha == 1
           if (!__all_sync(0xffffffffu, alpha == 1.0f)) {
@@ -1054,11 +1148,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&c->q_full[t]), 1);
       mbar_init(smem_u32(&c->q_empty[t]), 1);
-      mbar_init(smem_u32(&c->s_full[t]), 1);
+      mbar_init(smem_u32(&c->s_full[t][0]), 1);
+      mbar_init(smem_u32(&c->s_full[t][1]), 1);
       mbar_init(smem_u32(&c->p_full[t][0]), 8);
       mbar_init(smem_u32(&c->p_full[t][1]), 4);
+      mbar_init(smem_u32(&c->p_full[t][2]), 4);
       mbar_init(smem_u32(&c->sc_full[t]), 4);
       mbar_init(smem_u32(&c->o_full[t]), 1);
+      mbar_init(smem_u32(&c->pv_done[t]), 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&c->kv_full[s]), 1);
