@@ -63,6 +63,21 @@ def test_persistent_loop_more_items_than_sms(causal):
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["nc", "causal"])
+@pytest.mark.parametrize("N", [512, 640])
+def test_d64_s_buffers_across_items(N, causal):
+    """d = 64 uses its three S buffers in turn across all of a CTA's work
+    items.  At N = 512 and 640 an item's S count (n[0] + n[1]: 8 / 10
+    non-causal, 3 and 7 / 3, 7 and 10 causal) is not always a multiple of
+    three, so each item starts the rotation at another buffer; 400 heads
+    give every CTA several items of both kinds."""
+    inp = ai.make_inputs(1, 400, N, 64, "bf16", seed=31 + N)
+    o, lse = run_gpu(inp, causal)
+    heads = [(0, 0), (0, 1), (0, 151), (0, 152), (0, 303), (0, 399)]
+    compare(inp, causal, o, lse, heads=heads)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["nc", "causal"])
 def test_schedule_partial_reversed_round(causal):
     """200 work items on a 152-CTA grid: the second round runs in reversed
     CTA order and is only partly filled."""
