@@ -164,6 +164,40 @@ int attn_fwd_fp8_ws(const void* q, const void* k, const void* v, void* o, float*
                     void* workspace, unsigned long long workspace_bytes,
                     struct CUstream_st* stream);
 
+/* Options of attn_fwd_opt and attn_fwd_fp8_opt (bitwise OR). */
+#define ATTN_OPT_EXP2_FMA 1u
+
+/*
+ * attn_fwd_opt - attn_fwd with options.
+ *   ATTN_OPT_EXP2_FMA : 4 of every 32 softmax exponentials are computed on
+ *     the FMA pipe instead of the MUFU unit: x = n + f with n = round(x)
+ *     (Cody and Waite's reduction), 2^f by a degree-3 polynomial fitted
+ *     for the least largest relative error on [-1/2, 1/2] (7.5e-5 at most),
+ *     n added to the exponent; x < -126 gives 0.  The exponential unit is
+ *     the gap the "Inside FlashAttention-3 & Warp-Specialized CUDA Kernels"
+ *     page names in its introduction (MUFU.EX2 throughput against the
+ *     tensor cores); moving part of its work to the FMA pipe is this
+ *     library's own measure, off by default because it measured slower on
+ *     GB300 (the MUFU unit is not what bounds these kernels).  Built for
+ *     ATTN_BF16 with d = 64 or 128 and ATTN_FP8_E4M3 with d = 128; other
+ *     dtypes and head dims return ATTN_ERR_UNSUPPORTED.  No split of the
+ *     leftover work (no workspace).
+ *   opts = 0 is attn_fwd.  Unknown option bits are ATTN_ERR_INVALID_ARG.
+ * Other arguments, results and errors as attn_fwd.
+ */
+int attn_fwd_opt(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int causal, int dtype,
+                 unsigned int opts, struct CUstream_st* stream);
+
+/*
+ * attn_fwd_fp8_opt - attn_fwd_fp8 with the options of attn_fwd_opt
+ * (ATTN_OPT_EXP2_FMA is built for d = 128).
+ */
+int attn_fwd_fp8_opt(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int N, int d, float scale, int causal,
+                     float q_descale, float k_descale, float v_descale,
+                     unsigned int opts, struct CUstream_st* stream);
+
 /*
  * attn_fwd_fp8_blockscaled - forward pass on e4m3 Q and K that carry one
  * fp32 scale per 128-row tile of each (b, h) (the real value of a row in

@@ -28,10 +28,11 @@ GUARD = 256  # canary elements before and after each output
 
 
 def run_gpu(inp: ai.AttnInputs, causal: bool, guard: bool = True, split_tail=None,
-            workspace=None):
+            workspace=None, exp2_fma: bool = False):
     """Runs the library on the inputs (copied to cuda:0).  O and LSE are
     NaN-prefilled and surrounded by canaries; returns (O, LSE) on the CPU and
-    asserts the canaries are intact.  split_tail / workspace: as attn_fwd."""
+    asserts the canaries are intact.  split_tail / workspace / exp2_fma: as
+    attn_fwd."""
     dev = torch.device("cuda", 0)
     q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
     B, H, N, d = inp.shape
@@ -49,10 +50,10 @@ def run_gpu(inp: ai.AttnInputs, causal: bool, guard: bool = True, split_tail=Non
     if inp.dtype == "fp8":
         ws.attn_fwd_fp8(q, k, v, inp.descale["q"], inp.descale["k"], inp.descale["v"],
                         scale=inp.scale, causal=causal, out=o, lse=lse, split_tail=split_tail,
-                        workspace=workspace)
+                        workspace=workspace, exp2_fma=exp2_fma)
     else:
         ws.attn_fwd(q, k, v, scale=inp.scale, causal=causal, out=o, lse=lse,
-                    split_tail=split_tail, workspace=workspace)
+                    split_tail=split_tail, workspace=workspace, exp2_fma=exp2_fma)
     torch.cuda.synchronize()
     st = ws.attn_fwd_status()
     assert st == 0, f"watchdog status {ws.STATUS_NAMES.get(st, st)}"

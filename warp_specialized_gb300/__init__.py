@@ -18,10 +18,12 @@ __all__ = [
     "load_library", "attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_string",
     "attn_watchdog_selftest", "attn_fwd_raw", "attn_bwd", "attn_bwd_workspace_size",
     "attn_bwd_noalloc", "attn_fwd_fp8_blockscaled", "attn_quantize_fp8", "EXPORTED_SYMBOLS",
-    "attn_fwd_workspace_size", "attn_fwd_ws_raw", "attn_fwd_split_advised",
+    "attn_fwd_workspace_size", "attn_fwd_ws_raw", "attn_fwd_split_advised", "attn_fwd_opt_raw",
+    "ATTN_OPT_EXP2_FMA",
 ]
 
 ATTN_FP32, ATTN_FP16, ATTN_BF16, ATTN_FP8_E4M3 = 0, 1, 2, 3
+ATTN_OPT_EXP2_FMA = 1  # a share of the exponentials on the FMA pipe (attn_fwd_opt)
 
 STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
@@ -32,7 +34,7 @@ EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_status", "attn_status_
                     "attn_watchdog_selftest", "attn_bwd", "attn_bwd_workspace_size",
                     "attn_bwd_noalloc", "attn_fwd_fp8_blockscaled", "attn_quantize_fp8",
                     "attn_fwd_workspace_size", "attn_fwd_ws", "attn_fwd_fp8_ws",
-                    "attn_fwd_split_advised")
+                    "attn_fwd_split_advised", "attn_fwd_opt", "attn_fwd_fp8_opt")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -77,6 +79,11 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.attn_fwd_fp8_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, f, f, f, vp, u64,
                                         vp]
         lib.attn_fwd_fp8_ws.restype = i
+        lib.attn_fwd_opt.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, ctypes.c_uint, vp]
+        lib.attn_fwd_opt.restype = i
+        lib.attn_fwd_fp8_opt.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, f, f, f,
+                                         ctypes.c_uint, vp]
+        lib.attn_fwd_fp8_opt.restype = i
         lib.attn_fwd_split_advised.argtypes = [i, i, i, i, i, i]
         lib.attn_fwd_split_advised.restype = i
         lib.attn_fwd_status.argtypes = [vp]
@@ -140,6 +147,15 @@ def attn_fwd_ws_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int
                                       int(ws_bytes), stream)
 
 
+def attn_fwd_opt_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int,
+                     H: int, N: int, d: int, scale: float, causal: bool, dtype: int, opts: int,
+                     stream: int = 0) -> int:
+    """attn_fwd_opt with raw device pointers; returns the status code."""
+    return load_library().attn_fwd_opt(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d,
+                                       float(scale), int(bool(causal)), int(dtype), int(opts),
+                                       stream)
+
+
 def attn_fwd_workspace_size(d: int, dtype: int) -> int:
     """Bytes of workspace the forward's tail launch needs on the current device."""
     return int(load_library().attn_fwd_workspace_size(int(d), int(dtype)))
@@ -188,7 +204,7 @@ def _check_qkv(q, k, v):
 
 
 def attn_fwd(q, k, v, scale=None, causal: bool = False, out=None, lse=None, stream=None,
-             split_tail=None, workspace=None):
+             split_tail=None, workspace=None, exp2_fma: bool = False):
     """O, LSE = attention forward of [B, H, N, d] CUDA tensors.
 
     scale defaults to 1/sqrt(d).  out / lse may be given preallocated
@@ -198,7 +214,8 @@ def attn_fwd(q, k, v, scale=None, causal: bool = False, out=None, lse=None, stre
     (attn_fwd_ws), False never does, None (default) does where
     attn_fwd_split_advised says it pays; the split uses a uint8 `workspace`
     of at least attn_fwd_workspace_size(d, dtype) bytes, else one allocated
-    here.  Returns (out, lse)."""
+    here.  exp2_fma: ATTN_OPT_EXP2_FMA (attn_fwd_opt; bf16 d = 64 / 128, no
+    split).  Returns (out, lse)."""
     import torch
     _check_qkv(q, k, v)
     B, H, N, d = q.shape
@@ -211,9 +228,13 @@ def attn_fwd(q, k, v, scale=None, causal: bool = False, out=None, lse=None, stre
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     ws = None
-    if _use_split(split_tail, workspace, stream, B, H, N, d, causal, code):
+    if not exp2_fma and _use_split(split_tail, workspace, stream, B, H, N, d, causal, code):
         ws = _workspace(d, code, q.device, stream, workspace)
-    if ws is None:
+    if exp2_fma:
+        st = attn_fwd_opt_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), B, H, N, d, scale, causal, code,
+                              ATTN_OPT_EXP2_FMA, _stream_handle(stream))
+    elif ws is None:
         st = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                           lse.data_ptr(), B, H, N, d, scale, causal, code, _stream_handle(stream))
     else:
@@ -227,9 +248,9 @@ def attn_fwd(q, k, v, scale=None, causal: bool = False, out=None, lse=None, stre
 
 def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, scale=None,
                  causal: bool = False, out=None, lse=None, stream=None, split_tail=None,
-                 workspace=None):
+                 workspace=None, exp2_fma: bool = False):
     """Forward pass on e4m3 tensors with per-tensor descales; O is bf16.
-    split_tail and workspace as in attn_fwd."""
+    split_tail, workspace and exp2_fma as in attn_fwd (exp2_fma: d = 128)."""
     import torch
     _check_qkv(q, k, v)
     if q.dtype != torch.float8_e4m3fn:
@@ -245,9 +266,12 @@ def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, 
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d,
             float(scale), int(bool(causal)), float(q_descale), float(k_descale), float(v_descale))
     ws = None
-    if _use_split(split_tail, workspace, stream, B, H, N, d, causal, ATTN_FP8_E4M3):
+    if not exp2_fma and _use_split(split_tail, workspace, stream, B, H, N, d, causal,
+                                   ATTN_FP8_E4M3):
         ws = _workspace(d, ATTN_FP8_E4M3, q.device, stream, workspace)
-    if ws is None:
+    if exp2_fma:
+        st = lib.attn_fwd_fp8_opt(*args, ATTN_OPT_EXP2_FMA, _stream_handle(stream))
+    elif ws is None:
         st = lib.attn_fwd_fp8(*args, _stream_handle(stream))
     else:
         st = lib.attn_fwd_fp8_ws(*args, ws.data_ptr(), ws.numel(), _stream_handle(stream))

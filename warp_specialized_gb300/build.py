@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libattn_sm103.so")
 
-SOURCES = ["attn_api.cu", "inst_bf16.cu", "inst_fp16.cu", "inst_fp32.cu", "inst_fp8.cu",
+SOURCES = ["attn_api.cu", "inst_bf16.cu", "inst_fp16.cu", "inst_fp32.cu", "inst_fp8.cu", "inst_xf.cu",
            "attn_bwd.cu", "attn_bwd_noalloc.cu", "attn_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

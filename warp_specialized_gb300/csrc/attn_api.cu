@@ -125,9 +125,10 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
         int d, float scale, int causal, int dtype, float q_descale, float k_descale,
         float v_descale, cudaStream_t stream, const float* q_block_scale = nullptr,
         const float* k_block_scale = nullptr, void* workspace = nullptr,
-        unsigned long long workspace_bytes = 0ull) {
+        unsigned long long workspace_bytes = 0ull, unsigned int opts = 0u) {
   int rc = check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype);
   if (rc != kOk) return rc;
+  if (opts & ~static_cast<unsigned int>(ATTN_OPT_EXP2_FMA)) return kErrInvalidArg;
   if (workspace && !aligned(workspace, 256)) return kErrMisaligned;
   if (!finite_positive(q_descale) || !finite_positive(k_descale) || !finite_positive(v_descale))
     return kErrInvalidArg;
@@ -170,6 +171,7 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   a.encode = g_encode;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
+  if (opts & ATTN_OPT_EXP2_FMA) return workspace ? kErrInvalidArg : launch_exp2_fma(a, dtype);
   switch (dtype) {
     case ATTN_FP32: return launch_fp32(a);
     case ATTN_FP16: return launch_fp16(a);
@@ -275,6 +277,23 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
                  float v_descale, struct CUstream_st* stream) {
   return wsattn::run(q, k, v, o, lse, B, H, N, d, scale, causal, ATTN_FP8_E4M3, q_descale,
                      k_descale, v_descale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_opt(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, int dtype, unsigned int opts,
+                 struct CUstream_st* stream) {
+  return wsattn::run(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, 1.0f, 1.0f, 1.0f,
+                     reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, 0ull,
+                     opts);
+}
+
+int attn_fwd_fp8_opt(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, float scale, int causal, float q_descale,
+                     float k_descale, float v_descale, unsigned int opts,
+                     struct CUstream_st* stream) {
+  return wsattn::run(q, k, v, o, lse, B, H, N, d, scale, causal, ATTN_FP8_E4M3, q_descale,
+                     k_descale, v_descale, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                     nullptr, nullptr, 0ull, opts);
 }
 
 unsigned long long attn_fwd_workspace_size(int d, int dtype) {

@@ -766,11 +766,36 @@ constexpr int kRegsControl = 88;      // producer and MMA-issuer warpgroup
 constexpr int kRegsSoftmax = 168;     // each softmax warpgroup: a 128-score row
 constexpr int kRegsCorrection = 80;   // correction / epilogue warpgroup
 
+// 2^x for two values on the FMA pipe instead of MUFU (the optional path of
+// ATTN_OPT_EXP2_FMA).  Cody and Waite's reduction: x = n + f with n =
+// round(x), taken by adding and subtracting 1.5 * 2^23, and |f| <= 1/2;
+// then 2^f by a degree-3 polynomial and n added to its exponent field.  The
+// coefficients are the minimax fit of the relative error on [-1/2, 1/2]
+// that fit_exp2_poly.py computes (Remez exchange), 7.5e-5 at most.  x below
+// -126 (masked keys, x = -inf) gives exactly 0, as ex2.approx.ftz does.
+__device__ __forceinline__ void exp2_fma2(float x0, float x1, float& e0, float& e1) {
+  const uint64_t magic = f2_pack(12582912.f, 12582912.f);   // 1.5 * 2^23
+  const uint64_t xx = f2_pack(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
+  const uint64_t t2 = f2_add(xx, magic);                     // n in the low mantissa bits
+  const uint64_t n2 = f2_add(t2, f2_pack(-12582912.f, -12582912.f));
+  const uint64_t fr = f2_fma(n2, f2_pack(-1.f, -1.f), xx);   // f = x - n
+  uint64_t q = f2_fma(f2_pack(0.0551716685f, 0.0551716685f), fr,
+                      f2_pack(0.242611125f, 0.242611125f));
+  q = f2_fma(q, fr, f2_pack(0.693260968f, 0.693260968f));
+  q = f2_fma(q, fr, f2_pack(0.999928057f, 0.999928057f));
+  float q0, q1, t0, t1;
+  f2_unpack(q, q0, q1);
+  f2_unpack(t2, t0, t1);
+  e0 = x0 < -126.f ? 0.f : __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
+  e1 = x1 < -126.f ? 0.f : __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
+}
+
 // Exponentials of scores OFF .. OFF+LEN-1 of one row, written as P into
 // Tensor Memory at taddr_p (16-bit types pack two per column, e4m3 four).
-// x = s * scale_log2 - m in packed pairs, p = 2^x on MUFU.  Returns the sum
-// of the fp32 exponentials (before rounding to the P type).
-template <int DT, int OFF, int LEN>
+// x = s * scale_log2 - m in packed pairs, p = 2^x on MUFU, or, for XF of
+// every 32 scores (the last XF), on the FMA pipe (exp2_fma2).  Returns the
+// sum of the fp32 exponentials (before rounding to the P type).
+template <int DT, int OFF, int LEN, int XF = 0>
 __device__ __forceinline__ float exp_store_chunk(const float (&s)[128], float sl2, float neg_m,
                                                  uint32_t taddr_p) {
   const uint64_t k2 = f2_pack(sl2, sl2);
@@ -784,8 +809,16 @@ __device__ __forceinline__ float exp_store_chunk(const float (&s)[128], float sl
     float x0, x1, x2, x3;
     f2_unpack(f2_fma(f2_pack(s[i], s[i + 1]), k2, b2), x0, x1);
     f2_unpack(f2_fma(f2_pack(s[i + 2], s[i + 3]), k2, b2), x2, x3);
-    const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-    const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
+    float e0, e1, e2, e3;
+    if (XF > 0 && (ii % 32) >= 32 - XF) {
+      exp2_fma2(x0, x1, e0, e1);
+      exp2_fma2(x2, x3, e2, e3);
+    } else {
+      e0 = ex2_approx(x0);
+      e1 = ex2_approx(x1);
+      e2 = ex2_approx(x2);
+      e3 = ex2_approx(x3);
+    }
     acc0 = f2_add(acc0, f2_pack(e0, e1));
     acc1 = f2_add(acc1, f2_pack(e2, e3));
     if constexpr (DT == 3) {
@@ -816,7 +849,7 @@ __device__ __forceinline__ float exp_store_chunk(const float (&s)[128], float sl
 // that term exact.
 constexpr float kRescaleLog2 = 0.0f;
 
-template <int DT, int D, bool CAUSAL>
+template <int DT, int D, bool CAUSAL, int XF>
 __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
                              const AttnParams& p) {
   using C = Cfg<DT, D>;
@@ -913,12 +946,12 @@ __device__ void role_softmax(int t, Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase,
       // halves of 64 keys: the first is handed to the MMA issuer while the
       // second is computed
       const float neg_m = -m_use;
-      const float sum0 = exp_store_chunk<DT, 0, 64>(s, sl2j, neg_m, sa);
+      const float sum0 = exp_store_chunk<DT, 0, 64, XF>(s, sl2j, neg_m, sa);
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c->p_full[t][0]));
-      const float sum1 = exp_store_chunk<DT, 64, 64>(s, sl2j, neg_m, sa + C::kPCols / 2);
+      const float sum1 = exp_store_chunk<DT, 64, 64, XF>(s, sl2j, neg_m, sa + C::kPCols / 2);
       l_run = alpha * l_run + (sum0 + sum1);
       tmem_st_wait();
       // hand 1/l to the epilogue before the last P is announced
@@ -1125,7 +1158,9 @@ __device__ void role_correction(Ctrl<Cfg<DT, D>::kSlots>* c, uint32_t tbase, uin
 
 // ---------------------------------------------------------------------------
 
-template <int DT, int D, bool CAUSAL>
+// XF: exponentials of every 32 computed on the FMA pipe (0: all on MUFU;
+// the ATTN_OPT_EXP2_FMA instances use 4)
+template <int DT, int D, bool CAUSAL, int XF = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -1203,7 +1238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       role_mma<DT, D, CAUSAL>(sbase, c, tbase, p);
   } else if (wg == 1 || wg == 2) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    if (static_cast<int>(wg) - 1 < C::kNQT) role_softmax<DT, D, CAUSAL>(wg - 1, c, tbase, p);
+    if (static_cast<int>(wg) - 1 < C::kNQT) role_softmax<DT, D, CAUSAL, XF>(wg - 1, c, tbase, p);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCorrection));
     role_correction<DT, D, CAUSAL>(c, tbase, stage, &tmO, p);

@@ -85,10 +85,12 @@ inline int prepare_fwd_kernel(K kern, int smem_bytes, int device, std::atomic<in
   return st == 1 ? kOk : kErrUnsupported;
 }
 
-template <int DT, int D, bool CAUSAL>
+template <int DT, int D, bool CAUSAL, int XF = 0>
 int launch_instance(const LaunchArgs& a) {
   using C = Cfg<DT, D>;
-  auto kern = attn_fwd_kernel<DT, D, CAUSAL>;
+  auto kern = attn_fwd_kernel<DT, D, CAUSAL, XF>;
+  // the split tail runs the default (MUFU) exponentials only
+  constexpr bool kTail = !C::kQTmem && XF == 0;
   static std::atomic<int> ready[kMaxDevices], ready_tail[kMaxDevices];
   if (a.device < 0 || a.device >= kMaxDevices) return kErrDevice;
   int rc = prepare_fwd_kernel(kern, C::kSmemBytes, a.device, ready);
@@ -127,13 +129,13 @@ int launch_instance(const LaunchArgs& a) {
   // (d = 256 keeps its Q in Tensor Memory, a layout the tail kernel does not
   // have: it always runs whole items.)
   const TailPlan plan =
-      (a.workspace && !C::kQTmem)
+      (a.workspace && kTail)
           ? plan_tail(p.BH, p.n_pairs, p.nkv, C::kNQT, CAUSAL, a.num_sms,
                       tail_max_pieces(D, C::kEsize))
           : TailPlan{};
   const int tail = plan.items;
   const int tail_grid = plan.grid;
-  if constexpr (!C::kQTmem) {
+  if constexpr (kTail) {
   if (tail > 0) {
     rc = prepare_fwd_kernel(attn_fwd_tail_kernel<DT, D, CAUSAL>, TailCfg<DT, D>::kSmemBytes,
                             a.device, ready_tail);
@@ -170,7 +172,7 @@ int launch_instance(const LaunchArgs& a) {
       return kErrCuda;
     }
   }
-  if constexpr (!C::kQTmem) {
+  if constexpr (kTail) {
   if (tail > 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tail_grid, 1, 1);
@@ -201,6 +203,13 @@ int launch_instance(const LaunchArgs& a) {
 template <int DT, int D>
 int launch_mask(const LaunchArgs& a) {
   return a.causal ? launch_instance<DT, D, true>(a) : launch_instance<DT, D, false>(a);
+}
+
+// The instances of ATTN_OPT_EXP2_FMA: 4 exponentials of every 32 on the FMA
+// pipe.
+template <int DT, int D>
+int launch_mask_xf(const LaunchArgs& a) {
+  return a.causal ? launch_instance<DT, D, true, 4>(a) : launch_instance<DT, D, false, 4>(a);
 }
 
 }  // namespace wsattn

@@ -211,5 +211,7 @@ int launch_fp32(const LaunchArgs& a);
 int launch_fp16(const LaunchArgs& a);
 int launch_bf16(const LaunchArgs& a);
 int launch_fp8(const LaunchArgs& a);
+// ATTN_OPT_EXP2_FMA (bf16 d = 64 / 128, e4m3 d = 128; else kErrUnsupported)
+int launch_exp2_fma(const LaunchArgs& a, int dtype);
 
 }  // namespace wsattn

@@ -45,6 +45,9 @@ def main(argv=None):
                          "fp8_n8192_d128:nc,outlier_d64:bf16:causal (default: all)")
     ap.add_argument("--split", choices=["auto", "on", "off"], default="auto",
                     help="the forward's split tail launch: where it pays (auto), always, never")
+    ap.add_argument("--exp2-fma", action="store_true",
+                    help="time the forward with ATTN_OPT_EXP2_FMA (4 of every 32 exponentials "
+                         "on the FMA pipe; bf16 d = 64 / 128 and e4m3 d = 128)")
     ap.add_argument("--shape", default=None,
                     help="time only this forward shape B,H,N,d (bf16, N(0,1) inputs, both "
                          "masks unless --cases names one: e.g. --cases x:nc)")
@@ -108,7 +111,7 @@ def main(argv=None):
             B, H, N, d = inp.shape
             split = {"auto": None, "on": True, "off": False}[args.split]
             wsp = None
-            if split is not False:
+            if split is not False and not args.exp2_fma:
                 code = ws.ATTN_FP8_E4M3 if inp.dtype == "fp8" else ws.ATTN_BF16
                 wsp = torch.empty(ws.attn_fwd_workspace_size(d, code), dtype=torch.uint8,
                                   device="cuda")
@@ -120,13 +123,16 @@ def main(argv=None):
                     ds = inp.descale
                     fn = lambda: ws.attn_fwd_fp8(q, k, v, ds["q"], ds["k"], ds["v"],  # noqa: E731
                                                  scale=inp.scale, causal=causal, out=o, lse=lse,
-                                                 split_tail=split, workspace=wsp)
+                                                 split_tail=split, workspace=wsp,
+                                                 exp2_fma=args.exp2_fma)
                 else:
                     fn = lambda: ws.attn_fwd(q, k, v, scale=inp.scale, causal=causal,  # noqa: E731
-                                             out=o, lse=lse, split_tail=split, workspace=wsp)
+                                             out=o, lse=lse, split_tail=split, workspace=wsp,
+                                             exp2_fma=args.exp2_fma)
                 ms = median_ms(fn)
                 fl = ai.workload_flops(B, H, N, d, causal)
-                record(f"fwd {name}:{inp.dtype}:{'causal' if causal else 'nc'}",
+                record(f"fwd {name}:{inp.dtype}:{'causal' if causal else 'nc'}"
+                       + (":exp2_fma" if args.exp2_fma else ""),
                        ms=round(ms, 4), tflops=round(fl / ms / 1e9, 1))
             del q, k, v, o, lse, wsp
 
