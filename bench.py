@@ -144,12 +144,13 @@ def profiled_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock, power and throttle reasons."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clock, power and throttle reasons; only the
+    samples taken inside the timed region (by their timestamps) count."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 50):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.gpu = gpu_index
         self.period = period_ms
         self.proc = None
@@ -165,7 +166,41 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def summarise(lines, t_begin=None, t_end=None):
+        """Median SM clock, max clock and power, and the throttle reasons seen,
+        over the samples whose timestamps (host wall clock, seconds) lie in
+        [t_begin, t_end]; all samples when no window is given or none falls
+        in it (then "window" says so)."""
+        import datetime
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        parsed = []
+        for line in lines:
+            r = [x.strip() for x in line.split(",")]
+            if len(r) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                vals = (float(r[2]), float(r[3]), float(r[4]))
+            except ValueError:
+                continue
+            active = [n for n, v in zip(names, r[6:10]) if v.lower().startswith("active")]
+            parsed.append((ts, vals, active))
+        window = "timed region"
+        sel = parsed
+        if t_begin is not None:
+            sel = [p for p in parsed if t_begin <= p[0] <= t_end]
+            if not sel:
+                sel, window = parsed, "whole run (no sample inside the timed region)"
+        sm = [p[1][0] for p in sel]
+        reasons = sorted({n for p in sel for n in p[2]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(p[1][1] for p in sel) if sel else None,
+                "power_w_max": max(p[1][2] for p in sel) if sel else None,
+                "reasons": reasons, "samples": len(sel), "samples_total": len(parsed),
+                "window": window}
+
+    def stop(self, t_begin=None, t_end=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
                     "samples": 0}
@@ -175,24 +210,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.seek(0)
-        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.count(",") >= 8]
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [x.strip() for x in r]
-            try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-                power.append(float(r[3]))
-            except ValueError:
-                continue
-            for name, val in zip(names, r[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return self.summarise(self.out.read().strip().splitlines(), t_begin, t_end)
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -263,6 +281,7 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    t_begin = time.time()
     t0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()
@@ -271,9 +290,10 @@ def run_gpu(args):
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    t_end = time.time()
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_begin, t_end)
     if ws.attn_fwd_status() != 0:
         raise RuntimeError("watchdog fired during the timed region")
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]

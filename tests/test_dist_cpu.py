@@ -92,3 +92,27 @@ def test_check_world():
     cmd = bench.launch_command(8, ["--gpus", "8"], 29511)
     assert cmd[1:3] == ["-m", "torch.distributed.run"]
     assert "--nproc-per-node=8" in cmd and "127.0.0.1" in cmd and cmd[-2:] == ["--gpus", "8"]
+
+
+def test_clock_summary_counts_only_the_timed_region():
+    """The bench's clock record: samples outside the timed region (the idle
+    lead-in) do not count; a power-capped sample inside it does."""
+    import datetime
+
+    def ts(sec):
+        return datetime.datetime.fromtimestamp(sec).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+
+    t0 = 1_800_000_000.0
+    rows = [f"{ts(t0 + 0.02 * i)}, 0, 2070, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, "
+            "Not Active" for i in range(10)]
+    rows += [f"{ts(t0 + 0.3 + 0.02 * i)}, 0, {1950 if i > 2 else 2070}, 2070, 700.0, 0x4, "
+             f"Not Active, Not Active, Not Active, {'Active' if i > 2 else 'Not Active'}"
+             for i in range(7)]
+    s = bench.ClockSampler.summarise(rows, t0 + 0.29, t0 + 0.45)
+    assert s["samples"] == 7 and s["samples_total"] == 17 and s["window"] == "timed region"
+    assert s["reasons"] == ["sw_power_cap"] and s["sm_mhz"] == 1950.0
+    assert s["power_w_max"] == 700.0
+    whole = bench.ClockSampler.summarise(rows)
+    assert whole["samples"] == 17 and whole["sm_mhz"] == 2070.0
+    none_inside = bench.ClockSampler.summarise(rows, t0 + 5.0, t0 + 6.0)
+    assert none_inside["samples"] == 17 and none_inside["window"].startswith("whole run")
