@@ -15,7 +15,9 @@ sequences of both masks:
     yet (S(x) comes after P(x - 3) V);
   - a tile's S for block k + 2 is issued only after its P V for block k,
     which is what keeps a barrier kept in two sets from running two phases
-    ahead of its waiter.
+    ahead of its waiter, and what lets the softmax write alpha of block
+    k + 2 into the array of block k without waiting (that P V waited for
+    the correction warps' read of it).
 No GPU needed."""
 import random
 
