@@ -93,6 +93,7 @@ __device__ __forceinline__ void wht16_lanes(float (&v)[E]) {
       }
     }
   }
+  if constexpr (E >= 16) return;  // the whole group in this thread
   const int lane = static_cast<int>(threadIdx.x & 31);
 #pragma unroll
   for (int h = E; h < 16; h <<= 1) {
@@ -157,7 +158,9 @@ __device__ __forceinline__ void store_codes(const float (&v)[E], float b, float 
         __nv_cvt_float2_to_fp8x2(make_float2(q[4 * j + 2], q[4 * j + 3]), __NV_SATFINITE, __NV_E4M3);
     pk[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
   }
-  if constexpr (E == 8)
+  if constexpr (E == 16)
+    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  else if constexpr (E == 8)
     *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
   else
     *reinterpret_cast<uint32_t*>(dst) = pk[0];
@@ -171,12 +174,17 @@ __device__ __forceinline__ void store_codes(const float (&v)[E], float b, float 
 // the 16 / E chunks of a group of 16 channels sit in adjacent lanes.  The
 // tile is read once and kept in registers (raw words, or the rotated fp32
 // values) until the block maximum is known.
+//
+// With the rotation and 16-bit inputs a thread's chunk is 32 bytes (two
+// adjacent 16-byte loads): a whole group of 16 channels, so that the
+// butterfly runs without shuffles.
 template <typename T, int D, int NT, bool HAD>
 __global__ void __launch_bounds__(NT) quant_fp8_kernel(const T* __restrict__ x,
                                                       uint8_t* __restrict__ codes,
                                                       float* __restrict__ scales, int N,
                                                       int nt) {
-  constexpr int E = 16 / static_cast<int>(sizeof(T));  // channels per chunk
+  constexpr int kCV = HAD && sizeof(T) == 2 ? 2 : 1;    // 16-byte words per chunk
+  constexpr int E = 16 * kCV / static_cast<int>(sizeof(T));  // channels per chunk
   constexpr int W = D / E;                              // chunks per row
   constexpr int C = 128 * W / NT;                       // chunks per thread
   constexpr int kRowStep = NT / W;                      // rows between a thread's chunks
@@ -187,11 +195,24 @@ __global__ void __launch_bounds__(NT) quant_fp8_kernel(const T* __restrict__ x,
   const int tile = static_cast<int>(blk - bh * nt);
   const int row0 = tile * 128 + static_cast<int>(threadIdx.x) / W;
   const size_t base = (static_cast<size_t>(bh) * N + static_cast<size_t>(tile) * 128) * D;
-  const uint4* src = reinterpret_cast<const uint4*>(x + base) + threadIdx.x;
-  uint4 raw[C];
+  const uint4* src = reinterpret_cast<const uint4*>(x + base) + threadIdx.x * kCV;
+  uint4 raw[C][kCV];
 #pragma unroll
   for (int k = 0; k < C; ++k)
-    raw[k] = row0 + k * kRowStep < N ? src[k * NT] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < kCV; ++u)
+      raw[k][u] = row0 + k * kRowStep < N ? src[k * NT * kCV + u] : make_uint4(0u, 0u, 0u, 0u);
+  // the chunk's E values as fp32
+  constexpr int kPerWord = 16 / static_cast<int>(sizeof(T));
+  auto unpack = [&](int k, float (&v)[E]) {
+#pragma unroll
+    for (int u = 0; u < kCV; ++u) {
+      float w[kPerWord];
+      unpack_chunk<T>(raw[k][u], w);
+#pragma unroll
+      for (int i = 0; i < kPerWord; ++i) v[u * kPerWord + i] = w[i];
+    }
+  };
   // With 16-bit inputs the rotation's exact * 1/4 moves into the divisor:
   // value / scale = w / (4 scale) for value = w / 4, both exact, since w is
   // a multiple of the type's smallest step and stays far from fp32's
@@ -206,10 +227,10 @@ __global__ void __launch_bounds__(NT) quant_fp8_kernel(const T* __restrict__ x,
     uint32_t m2 = 0u;
 #pragma unroll
     for (int k = 0; k < C; ++k) {
-      m2 = __vmaxu2(m2, raw[k].x & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, raw[k].y & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, raw[k].z & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, raw[k].w & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, raw[k][0].x & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, raw[k][0].y & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, raw[k][0].z & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, raw[k][0].w & 0x7FFF7FFFu);
     }
     const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
     if constexpr (std::is_same<T, __half>::value)
@@ -220,7 +241,7 @@ __global__ void __launch_bounds__(NT) quant_fp8_kernel(const T* __restrict__ x,
 #pragma unroll
     for (int k = 0; k < C; ++k) {
       float v[E];
-      unpack_chunk<T>(raw[k], v);
+      unpack(k, v);
       if constexpr (HAD) {
         wht16_lanes<E>(v);
 #pragma unroll
@@ -257,7 +278,7 @@ __global__ void __launch_bounds__(NT) quant_fp8_kernel(const T* __restrict__ x,
 #pragma unroll
         for (int i = 0; i < E; ++i) v[i] = rot[k][i];
       } else {
-        unpack_chunk<T>(raw[k], v);
+        unpack(k, v);
       }
       store_codes<E, kRefine>(v, div, y, dst + static_cast<size_t>(k) * NT * E);
     }
@@ -273,7 +294,8 @@ int launch_quant(const void* x, void* codes, float* scales, int B, int H, int N,
                  cudaStream_t stream) {
   // Four 16-byte chunks per thread for 16-bit rows and eight for fp32 rows
   // (capped at 512 threads) measured fastest: bf16 d = 128 takes 512
-  // threads, d = 64 takes 256.
+  // threads, d = 64 takes 256.  (With the rotation a 16-bit thread holds the
+  // same bytes as two 32-byte chunks.)
   constexpr int kW = D * static_cast<int>(sizeof(T)) / 16;
   constexpr int kPerThread = sizeof(T) == 4 ? 8 : 4;
   constexpr int kNT = 128 * kW / kPerThread > 512 ? 512 : 128 * kW / kPerThread;
