@@ -33,6 +33,9 @@ SMALL = [
     (1, 2, 640, 128, "bf16"),
     (1, 2, 333, 64, "bf16"),
     (1, 2, 256, 64, "fp16"),
+    (1, 2, 1, 64, "bf16"),
+    (1, 2, 100, 64, "bf16"),
+    (1, 2, 129, 64, "fp16"),
     (1, 2, 333, 256, "bf16"),
     (1, 2, 256, 256, "fp16"),
     (1, 2, 200, 128, "fp16"),
@@ -63,13 +66,14 @@ def test_persistent_loop_more_items_than_sms(causal):
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["nc", "causal"])
-@pytest.mark.parametrize("N", [512, 640])
+@pytest.mark.parametrize("N", [128, 512, 640])
 def test_d64_s_buffers_across_items(N, causal):
     """d = 64 uses its three S buffers in turn across all of a CTA's work
     items.  At N = 512 and 640 an item's S count (n[0] + n[1]: 8 / 10
     non-causal, 3 and 7 / 3, 7 and 10 causal) is not always a multiple of
-    three, so each item starts the rotation at another buffer; 400 heads
-    give every CTA several items of both kinds."""
+    three, so each item starts the rotation at another buffer; at N = 128
+    every item is one block (two S products, none issued ahead); 400 heads
+    give every CTA several items."""
     inp = ai.make_inputs(1, 400, N, 64, "bf16", seed=31 + N)
     o, lse = run_gpu(inp, causal)
     heads = [(0, 0), (0, 1), (0, 151), (0, 152), (0, 303), (0, 399)]
